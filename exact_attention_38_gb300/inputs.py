@@ -1,0 +1,47 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
+
+This module holds no attention arithmetic: it only draws random numbers.  Recipe
+(the pages name no generator; only the small fp16 case fixes seed 0): a CPU
+``torch.Generator`` seeded with ``seed`` draws fp32 standard normals for q, k, v
+and then dO, in that order, with shapes [B, N, Hq, d], [B, N, Hkv, d],
+[B, N, Hkv, d], [B, N, Hq, d]; each is rounded to nearest into the 16-bit dtype.
+The workload family is the one the FlashAttention-2 pages benchmark
+(iid N(0,1) activations, head dim 64 or 128, 16k tokens per batch).
+"""
+
+from __future__ import annotations
+
+import torch
+
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def make_inputs(B, N, Hq, Hkv, d, dtype="bf16", seed=0, with_do=True, special=None):
+    """Return a dict of CPU tensors q, k, v (and do) in the 16-bit ``dtype``.
+
+    ``special`` optionally overrides the draw to build closed-form cases:
+    "v_ones" sets V to 1, "q_zero" sets Q to 0 (the draw order is unchanged).
+    """
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((B, N, Hq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, N, Hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, N, Hkv, d), generator=g, dtype=torch.float32)
+    out = {}
+    if with_do:
+        out["do"] = torch.randn((B, N, Hq, d), generator=g, dtype=torch.float32).to(tdt)
+    if special == "v_ones":
+        v = torch.ones_like(v)
+    elif special == "q_zero":
+        q = torch.zeros_like(q)
+    elif special is not None:
+        raise ValueError(f"unknown special case {special!r}")
+    out["q"] = q.to(tdt)
+    out["k"] = k.to(tdt)
+    out["v"] = v.to(tdt)
+    return out
+
+
+def to_f64(t):
+    """Exact upcast of a 16-bit CPU tensor to a float64 numpy array."""
+    return t.detach().to("cpu", torch.float64).numpy()
