@@ -1,0 +1,343 @@
+"""Benchmark of the attention hot path: one step = forward + backward through libfa.so.
+
+Workload (the pages' benchmark family at 16k tokens per batch, head dim 128):
+B=1, Hq=Hkv=16, N=16384, d=128, bf16 inputs iid N(0,1), scale=1/sqrt(d), non-causal.
+FLOPs per step = 4*B*Hq*N^2*d (forward) * 3.5 (forward + backward at 2.5x forward),
+halved for causal.  Prints ONE JSON line (see the keys below).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--causal] [--pass step|fwd|bwd]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Multi-GPU: the path shards with no exchange step; under torchrun each rank runs an
+independent replica of the workload ("weak" scaling), `value` sums all ranks' work over
+the max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s at 16k tokens/batch; % of GB300 BF16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--pass", dest="which", default="step", choices=["step", "fwd", "bwd"])
+    ap.add_argument("--N", type=int, default=16384)
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload(a):
+    B = a.B if a.B is not None else max(1, 16384 // a.N)
+    return dict(B=B, Hq=a.H, Hkv=a.H, N=a.N, d=a.d, causal=bool(a.causal), dtype="bf16")
+
+
+def flops(w, which):
+    f = 4.0 * w["B"] * w["Hq"] * w["N"] ** 2 * w["d"]
+    if w["causal"]:
+        f /= 2
+    return {"fwd": f, "bwd": 2.5 * f, "step": 3.5 * f}[which]
+
+
+def workload_name(w, which):
+    passes = {"step": "fwd+bwd", "fwd": "fwd", "bwd": "bwd"}[which]
+    return (f"exact attention {passes}, B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} N={w['N']} d={w['d']} "
+            f"{w['dtype']} {'causal' if w['causal'] else 'non-causal'} (16k tokens/batch)")
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j.get("bf16_tflops"), j.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+# ----------------------------------------------------------- clocks during timing
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU baseline
+
+def cpu_oracle_sample(w, steps=1):
+    """The fp64 oracle, as it stands, on a bounded slice of the same workload."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_38_gb300.inputs import make_inputs, to_f64
+
+    cores = len(os.sched_getaffinity(0))
+    n_s, heads = min(w["N"], 4096), min(w["Hq"], 4)
+    x = make_inputs(1, n_s, heads, heads, w["d"], dtype=w["dtype"], seed=3)
+    xo = {k: to_f64(v) for k, v in x.items()}
+    scale = 1.0 / math.sqrt(w["d"])
+    fl = 3.5 * 4.0 * heads * n_s ** 2 * w["d"] * (0.5 if w["causal"] else 1.0)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        r = oracle.attn_bwd_ref(xo["q"], xo["k"], xo["v"], xo["do"], w["causal"], scale)
+        times.append(time.perf_counter() - t0)
+        assert np.isfinite(r["dq"]).all()
+    sample = (f"oracle attn_bwd_ref (fwd+all grads, fp64 numpy) on B=1, {heads} heads, N={n_s}, d={w['d']} "
+              f"({'causal' if w['causal'] else 'non-causal'}); FLOPs by the same formula")
+    return fl, times, cores, sample
+
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(a)
+    fl, times, cores, sample = cpu_oracle_sample(w, steps=a.warmup + a.steps)
+    t = times[a.warmup:] if len(times) > a.warmup else times
+    sec = sum(t) / len(t)
+    val = fl / sec / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(w, "step") + " [oracle runs a bounded slice, see cpu_baseline]",
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- native
+
+def run_native(a):
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_38_gb300 import fa
+    from exact_attention_38_gb300.inputs import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload(a)
+    B, Hq, Hkv, N, d, causal = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    x = make_inputs(B, N, Hq, Hkv, d, dtype=w["dtype"], seed=3 + rank)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_size(B, Hq, Hkv, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    DT = fa.FA_BF16
+
+    def fwd():
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, d,
+                       causal, scale, DT, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd")
+
+    def bwd():
+        st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, scale, DT,
+                       ws.data_ptr(), ws_bytes, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd")
+
+    parts = {"step": [("fwd", fwd), ("bwd", bwd)], "fwd": [("fwd", fwd)], "bwd": [("bwd", bwd)]}[a.which]
+    if a.which == "bwd":
+        fwd()
+    launches_per_step = sum({"fwd": 1, "bwd": 3}[n] for n, _ in parts)
+
+    for _ in range(a.warmup):
+        for _, fn in parts:
+            fn()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+
+    K = a.steps
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n, _ in parts}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.zero_()  # evict the previous step's data from L2 (outside the events)
+            for n, fn in parts:
+                ev[n][i][0].record(stream)
+                fn()
+                ev[n][i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    fa.check_device_error()
+    per = {n: [e0.elapsed_time(e1) for e0, e1 in ev[n]] for n in ev}
+    ms_step = sum(statistics.mean(per[n]) for n in per)
+    t_max = torch.tensor([ms_step], device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    ms_step = float(t_max.item())
+    fl_step = flops(w, a.which)
+    value = world * fl_step / (ms_step * 1e-3) / 1e12
+
+    # ---- e2e: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not a.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (x["q"], x["k"], x["v"], x["do"]))
+        ho, hdq, hdk, hdv = (torch.empty_like(t, device="cpu").pin_memory() for t in (hq, hq, hk, hv))
+        hlse = torch.empty((B, Hq, N), dtype=torch.float32).pin_memory()
+        ins = [(hq, q), (hk, k), (hv, v), (hdo, do)]
+        outs = [(ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)]
+        if a.which == "fwd":
+            ins, outs = ins[:3], outs[:2]
+        h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+        d2h = sum(t.numel() * t.element_size() for t, _ in outs)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for rep in range(2):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(K):
+                for h_, d_ in ins:
+                    d_.copy_(h_, non_blocking=True)
+                for _, fn in parts:
+                    fn()
+                for h_, d_ in outs:
+                    h_.copy_(d_, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / K
+        t2 = torch.tensor([ms_e2e], device=dev)
+        if world > 1:
+            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * fl_step / (float(t2.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(t2.item())}
+        fa.check_device_error()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak_tf, peak_hbm, peak_kind = measured_peaks()
+    # dominant kernel: the pass with the largest share of the step
+    dom = max(per, key=lambda n: statistics.mean(per[n]))
+    dom_ms = statistics.mean(per[dom])
+    achieved = flops(w, dom) / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel" if dom == "fwd" else "fa_bwd (3 launches)",
+                "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                "traffic": None, "peak_kind": f"{peak_kind} bf16 dense (burst)"}
+    passes = {n: {"ms": statistics.mean(per[n]), "ms_min": min(per[n]),
+                  "tflops": flops(w, n) / (statistics.mean(per[n]) * 1e-3) / 1e12} for n in per}
+    for n in passes:
+        passes[n]["frac_of_peak"] = passes[n]["tflops"] / peak_tf
+
+    cpu = None
+    if not a.no_cpu_baseline:
+        fl_s, times, cores, sample = cpu_oracle_sample(w, steps=1)
+        cpu = {"value": fl_s / times[0] / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": sample, "seconds": times[0]}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": a.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(w, a.which), "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                       "causal": causal, "global_batch": B * world, "seq_len": N,
+                       "parallelism": f"replicas x{world} (no exchange step)",
+                       "l2": "flushed between steps (2x L2 buffer written outside the timed events); "
+                             "inputs (q,k,v,dO,o = 320 MiB) also exceed L2"},
+            "passes": passes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * K, "wall_s_timed_region": t_wall,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_native(a)
+
+
+if __name__ == "__main__":
+    main()

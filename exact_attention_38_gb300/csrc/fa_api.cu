@@ -1,0 +1,166 @@
+// C ABI of libfa.so: argument validation, tensor-map encoding, launches.
+// Every argument check happens before the first CUDA call, so a bad call returns
+// an error code without touching the device (and works on a host without a GPU).
+#include "fa_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace fa {
+
+__device__ unsigned g_fa_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned*> g_err_ptr[kMaxDevices];
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  PFN_cuTensorMapEncodeTiled_v12000 f = g_encode.load(std::memory_order_acquire);
+  if (f) return f;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return nullptr;
+  f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  g_encode.store(f, std::memory_order_release);
+  return f;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by forward and backward.
+fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return FA_ERR_INVALID;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (N > (1 << 20)) return FA_ERR_UNSUPPORTED;
+  // element counts must fit the tensor maps and 2^31 CTAs
+  const long long rows = static_cast<long long>(B) * N;
+  if (rows * Hq * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  const long long tiles = static_cast<long long>(B) * Hq * ((N + 255) / 256);
+  if (tiles >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_fa_error_word) != cudaSuccess) return nullptr;
+  p = static_cast<unsigned*>(addr);
+  g_err_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
+                     fa_dtype dtype) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t es = 2;
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(H) * d * es,
+                                 static_cast<cuuint64_t>(N) * H * d * es};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid but unsupported size or head dimension";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel's bounded wait ran out";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                 int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+  const fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  FwdParams p{};
+  if (!encode_bshd_map(&p.tm_q, q, B, N, Hq, d, 128, dtype) || !encode_bshd_map(&p.tm_k, k, B, N, Hkv, d, 128, dtype) ||
+      !encode_bshd_map(&p.tm_v, v, B, N, Hkv, d, 128, dtype) || !encode_bshd_map(&p.tm_o, o, B, N, Hq, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_fwd(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * N * Hq;
+  const size_t dq_bytes = (rows * d * 4 + 255) & ~size_t(255);
+  const size_t d_bytes = (rows * 4 + 255) & ~size_t(255);
+  return dq_bytes + d_bytes;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  const fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  if (workspace_bytes < fa_bwd_workspace_size(B, Hq, Hkv, N, d)) return FA_ERR_INVALID;
+  (void)causal;
+  (void)stream;
+  return FA_ERR_UNSUPPORTED;
+}
+
+fa_status fa_check_device_error(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned* w = device_error_word();
+  if (!w) return FA_ERR_CUDA;
+  unsigned h = 0;
+  if (cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (h != 0) {
+    const unsigned z = 0;
+    if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

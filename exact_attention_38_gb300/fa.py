@@ -1,0 +1,142 @@
+"""ctypes binding of libfa.so: argument marshalling only, every step runs in the library.
+
+The C names are mirrored one to one (``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``,
+``fa_check_device_error``, ``fa_status_string``).  ``forward`` / ``backward`` are
+conveniences that allocate the outputs with torch (device memory and streams are
+the only things torch provides here) and call the C entry points on the current
+stream.  Importing this module loads the library and raises if it is missing: there
+is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_BF16, FA_FP16 = 0, 1
+_DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libfa.so not found at {LIB_PATH}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_check_device_error.argtypes = [vp]
+    lib.fa_check_device_error.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------- raw C entry points
+
+def status_string(status: int) -> str:
+    return lib.fa_status_string(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype, stream) -> int:
+    """Mirror of the C ``fa_fwd``; pointers and stream are plain integers."""
+    return lib.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, int(causal), float(scale), int(dtype), stream)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, workspace,
+           workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_bwd``."""
+    return lib.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
+                      int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_workspace_size(B, Hq, Hkv, N, d) -> int:
+    return int(lib.fa_bwd_workspace_size(B, Hq, Hkv, N, d))
+
+
+def fa_check_device_error(stream) -> int:
+    return lib.fa_check_device_error(stream)
+
+
+# ------------------------------------------------------------------- conveniences
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, N, H, d]")
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    if q.dtype not in _DT:
+        raise ValueError("dtype must be bf16 or fp16")
+    return B, N, Hq, Hkv, d
+
+
+def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """Returns (o [B,N,Hq,d], lse [B,Hq,N] fp32)."""
+    B, N, Hq, Hkv, d = _shapes(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, causal, scale, _DT[q.dtype],
+                _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def backward(dout, q, k, v, o, lse, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
+             stream=None):
+    """Returns (dq, dk, dv); allocates the workspace with torch if not given."""
+    B, N, Hq, Hkv, d = _shapes(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                Hkv, N, d, causal, scale, _DT[q.dtype], _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def check_device_error(stream=None):
+    st = fa_check_device_error(_stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_check_device_error")

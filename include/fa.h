@@ -1,0 +1,116 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library, libfa.so.
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ *
+ * tile by tile with the online softmax (running row maximum and row sum, partial
+ * outputs rescaled as the maximum grows), so the N x N score and probability
+ * matrices never reach device memory; and its backward pass.  The method is the one
+ * described in "FlashAttention-2: atención eficiente en GPU para contextos largos"
+ * (sections "El coste de mover datos en secuencias largas", "Bloques pequeños,
+ * normalización global" and "Tres mejoras en la utilización de la GPU"): exact
+ * attention, results equal to the plain definition up to floating-point rounding
+ * order, forward and backward, with and without a causal mask.  Grouped-query
+ * attention follows "FlashAttention-T: Optimización GPU para LLMs Escalables"
+ * (section "Innovaciones técnicas frente a FlashAttention original").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers on the current CUDA device, owned and
+ *    allocated by the caller; the library never allocates or frees device memory
+ *    during a call.  Every pointer must be 16-byte aligned (tensor-memory-access
+ *    copies require it).
+ *  - Layouts (row-major, last index fastest, all contiguous):
+ *        q, o, dq, dout : [B, N, Hq,  d]     16-bit (see fa_dtype)
+ *        k, v, dk, dv   : [B, N, Hkv, d]     16-bit
+ *        lse            : [B, Hq, N]         fp32, natural-log log-sum-exp of the
+ *                                            SCALED scores of each query row
+ *  - Query head h reads key/value head h / (Hq / Hkv) (contiguous groups).
+ *  - Causal: key j is visible to query i iff j <= i (queries and keys share N, the
+ *    mask is aligned at the top-left corner).
+ *  - Supported: d in {64, 128}; 1 <= N <= 2^20; B, Hq, Hkv >= 1; Hq % Hkv == 0;
+ *    scale finite and > 0.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are reported synchronously, before any
+ *    work is enqueued.  Errors inside a kernel (a bounded wait that ran out) are
+ *    recorded in a per-device error word that fa_check_device_error() reads.
+ *  - Calls on different streams may overlap; the library keeps no per-call state.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (binary-compatible with cudaStream_t / CUstream). */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,     /* bad argument: null/misaligned pointer, bad size, Hq % Hkv != 0 */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented: d not in {64,128}, N too large */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or kernel launch failed */
+  FA_ERR_TIMEOUT = 4      /* a kernel's bounded wait ran out (reported by fa_check_device_error) */
+} fa_status;
+
+typedef enum fa_dtype { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/*
+ * Forward pass.
+ *   q [B,N,Hq,d], k/v [B,N,Hkv,d] (inputs, dtype), o [B,N,Hq,d] (output, dtype),
+ *   lse [B,Hq,N] (output, fp32; needed by fa_bwd).
+ *   scale multiplies the scores before the softmax (1/sqrt(d) for standard attention).
+ * O is rounded to nearest into `dtype` from an fp32 accumulator.  The kernel is
+ * exact attention: it differs from the plain definition only by rounding
+ * ("Bloques pequeños, normalización global").
+ * Returns FA_OK once the work is enqueued.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                 int N, int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes (fp32 dQ accumulator
+ * [B,N,Hq,d] plus D = rowsum(dO * O) [B,Hq,N], each rounded up to 256 bytes).
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * Backward pass: gradients of L = sum(dout * o) with respect to q, k and v.
+ *   q, k, v, o, lse : the forward's inputs and outputs (o and lse from fa_fwd with
+ *                     the same q, k, v, causal and scale)
+ *   dout            : [B,N,Hq,d] upstream gradient dO (dtype)
+ *   dq [B,N,Hq,d], dk/dv [B,N,Hkv,d] : outputs (dtype), fully overwritten; dk and
+ *                     dv of a key/value head sum over the query heads of its group
+ *   workspace       : device scratch of at least fa_bwd_workspace_size() bytes,
+ *                     256-byte aligned; its contents on entry do not matter and
+ *                     it must not be shared by calls that may overlap.
+ * The pass runs D = rowsum(dO * O), then a kernel over key blocks that recomputes
+ * P from lse, accumulates dV and dK in tensor memory and adds dS K into the fp32
+ * dQ accumulator, then converts dQ to dtype.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                 int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting and wound down without
+ * finishing its work; its outputs are undefined) or FA_ERR_CUDA.
+ */
+fa_status fa_check_device_error(fa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

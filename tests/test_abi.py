@@ -1,0 +1,103 @@
+"""The C ABI library loads on a host without a GPU, exports every entry point that
+include/fa.h declares, and rejects bad arguments before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+LIB = os.path.join(ROOT, "exact_attention_38_gb300", "libfa.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from exact_attention_38_gb300 import build
+
+        build.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_error", "fa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    for code, word in [(0, b"FA_OK"), (1, b"INVALID"), (2, b"UNSUPPORTED"), (3, b"CUDA"), (4, b"TIMEOUT")]:
+        assert word in lib.fa_status_string(code)
+
+
+def _fwd(lib, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, B=1, Hq=2, Hkv=2, N=128, d=64,
+             causal=0, scale=0.125, dtype=0)
+    a.update(kw)
+    f = lib.fa_fwd
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, vp]
+    f.restype = i
+    return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["causal"],
+             a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=0x20008), 1), (dict(lse=0x50004), 1),
+    (dict(N=0), 1), (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(Hkv=0), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(dtype=7), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1), (dict(N=(1 << 20) + 1), 2),
+])
+def test_fwd_argument_errors_need_no_device(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _bwd(lib, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, do=0x60000, dq=0x70000, dk=0x80000,
+             dv=0x90000, B=1, Hq=4, Hkv=2, N=300, d=128, causal=1, scale=0.088, dtype=0, ws=0x100000,
+             ws_bytes=None)
+    a.update(kw)
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 5
+    need = lib.fa_bwd_workspace_size(a["B"], a["Hq"], a["Hkv"], a["N"], a["d"])
+    ws_bytes = need if a["ws_bytes"] is None else a["ws_bytes"]
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f = lib.fa_bwd
+    f.argtypes = [vp] * 9 + [i] * 6 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+    f.restype = i
+    return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["B"], a["Hq"],
+             a["Hkv"], a["N"], a["d"], a["causal"], a["scale"], a["dtype"], a["ws"], ws_bytes, None)
+
+
+def test_workspace_size(lib):
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 5
+    B, Hq, N, d = 2, 4, 300, 128
+    rows = B * Hq * N
+    want = ((rows * d * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert lib.fa_bwd_workspace_size(B, Hq, 2, N, d) == want
+    assert lib.fa_bwd_workspace_size(B, Hq, 3, N, d) == 0
+    assert lib.fa_bwd_workspace_size(B, Hq, 2, N, 80) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(do=None), 1), (dict(dk=0x80002), 1), (dict(ws=None), 1), (dict(ws=0x100010), 1),
+    (dict(ws_bytes=1024), 1), (dict(Hq=5), 1), (dict(d=32), 2), (dict(N=-5), 1),
+])
+def test_bwd_argument_errors_need_no_device(lib, kw, code):
+    assert _bwd(lib, **kw) == code
