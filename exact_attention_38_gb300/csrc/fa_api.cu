@@ -56,6 +56,18 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int dty
 
 }  // namespace
 
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t rows = static_cast<size_t>(B) * N * Hq;
+  const size_t npad = (static_cast<size_t>(N) + 63) / 64 * 64;
+  BwdWorkspace w{};
+  w.dq_acc_off = 0;
+  w.dvec_off = up(rows * d * 4);
+  w.l2vec_off = w.dvec_off + up(static_cast<size_t>(B) * Hq * npad * 4);
+  w.total = w.l2vec_off + up(static_cast<size_t>(B) * Hq * npad * 4);
+  return w;
+}
+
 unsigned* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -128,10 +140,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
   if (check_sizes(B, Hq, Hkv, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
-  const size_t rows = static_cast<size_t>(B) * N * Hq;
-  const size_t dq_bytes = (rows * d * 4 + 255) & ~size_t(255);
-  const size_t d_bytes = (rows * 4 + 255) & ~size_t(255);
-  return dq_bytes + d_bytes;
+  return bwd_workspace_layout(B, Hq, N, d).total;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
@@ -143,10 +152,34 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
   const fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, static_cast<int>(dtype));
   if (st != FA_OK) return st;
-  if (workspace_bytes < fa_bwd_workspace_size(B, Hq, Hkv, N, d)) return FA_ERR_INVALID;
-  (void)causal;
-  (void)stream;
-  return FA_ERR_UNSUPPORTED;
+  const BwdWorkspace ws = bwd_workspace_layout(B, Hq, N, d);
+  if (workspace_bytes < ws.total) return FA_ERR_INVALID;
+  BwdParams p{};
+  if (!encode_bshd_map(&p.tm_q, q, B, N, Hq, d, 64, dtype) || !encode_bshd_map(&p.tm_do, dout, B, N, Hq, d, 64, dtype) ||
+      !encode_bshd_map(&p.tm_k, k, B, N, Hkv, d, 128, dtype) || !encode_bshd_map(&p.tm_v, v, B, N, Hkv, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
+  p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
+  p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.Npad = (N + 63) / 64 * 64;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_check_device_error(fa_stream_t stream) {

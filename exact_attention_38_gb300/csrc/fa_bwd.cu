@@ -1,0 +1,539 @@
+// Backward pass of exact attention on sm_103a: dQ, dK, dV of L = sum(dO * O).
+//
+// The pages ask for gradients equal to the plain definition's within tolerance
+// ("FlashAttention-2: atención eficiente en GPU para contextos largos", section
+// "Bloques pequeños, normalización global") and a backward "almost as fast as the
+// forward" with MQA/GQA ("FlashAttention-T: Optimización GPU para LLMs Escalables",
+// section "Innovaciones técnicas frente a FlashAttention original").  The pass is the
+// textbook gradient evaluated tile by tile, recomputing P from the saved log-sum-exp
+// instead of storing it:
+//
+//   D_i    = <dO_i, O_i>                                   (fa_bwd_preprocess)
+//   P_ij   = exp(scale * q_i.k_j - lse_i)
+//   dV_j  += sum_i P_ij dO_i
+//   dS_ij  = P_ij (dO_i.v_j - D_i)
+//   dK_j  += scale * sum_i dS_ij q_i
+//   dQ_i  += scale * sum_j dS_ij k_j                       (fp32 workspace, then fa_bwd_dq_convert)
+//
+// fa_bwd_main: one CTA per (batch, key/value head, block of 128 keys).  K_j and V_j stay
+// in shared memory; the CTA walks every query head of its GQA group and every visible
+// block of 64 queries.  Per step the tensor cores compute S^T = K Q^T and dP^T = V dO^T
+// into tensor memory (S^T double-buffered), a softmax warpgroup (thread = key row =
+// TMEM lane) turns them into P^T (written back to TMEM as 16-bit pairs) and dS^T
+// (written to swizzled shared memory), and the tensor cores then accumulate
+// dV += P^T dO and dK += dS^T Q in TMEM for the whole walk and compute
+// dQ^T = K^T dS^T, which a second warpgroup adds into the fp32 dQ accumulator with
+// coalesced reductions while the next step's S^T / dP^T run.
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+
+#include <cuda_fp16.h>
+
+namespace fa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BK = 128;                  // keys per CTA (TMEM lanes)
+  static constexpr int BQ = 64;                   // queries per step
+  static constexpr int CHUNKS = D / 64;           // 128-byte swizzle column chunks
+  static constexpr int KV_TILE = 128 * D * 2;     // K or V tile
+  static constexpr int KV_CHUNK = 128 * 128;      // 128 rows x 128 B
+  static constexpr int Q_CHUNK = 64 * 128;        // 64 rows x 128 B
+  static constexpr int Q_TILE = 64 * D * 2;       // Q or dO tile
+  static constexpr int DS_TILE = 128 * 64 * 2;    // dS^T tile, 128 keys x 64 queries, 16-bit
+  static constexpr int STG = (D == 128) ? 3 : 5;  // Q/dO/lse/D stages
+  static constexpr int THREADS = 384;
+  // barrier indices
+  static constexpr int B_KV = 0, B_SDP = 1, B_DPFREE = 2, B_DSREADY = 3 /*[2]*/, B_DSFREE = 5 /*[2]*/,
+                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_STFULL = 11 /*[STG]*/;
+  static constexpr int NBARS = 11 + 2 * STG;
+  // shared-memory layout (offsets from the 1024-aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_TILE;
+  static constexpr int OFF_Q = 2 * KV_TILE;                    // [STG] Q tiles
+  static constexpr int OFF_DO = OFF_Q + STG * Q_TILE;          // [STG] dO tiles
+  static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles
+  static constexpr int OFF_LD = OFF_DS + 2 * DS_TILE;          // [STG][2][64] floats: lse*log2e, D
+  static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 8 * NBARS + 64;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  // tensor-memory columns
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+__device__ __forceinline__ float bw_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t bw_pack2(float lo, float hi) {
+  uint32_t r;
+  if (BF16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float bw_unpack_lo(uint32_t v) {
+  if (BF16) return __uint_as_float(v << 16);
+  __half_raw hr;
+  hr.x = static_cast<unsigned short>(v & 0xFFFFu);
+  return __half2float(__half(hr));
+}
+
+template <bool BF16>
+__device__ __forceinline__ float bw_unpack_hi(uint32_t v) {
+  if (BF16) return __uint_as_float(v & 0xFFFF0000u);
+  __half_raw hr;
+  hr.x = static_cast<unsigned short>(v >> 16);
+  return __half2float(__half(hr));
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------------- preprocess
+// D = rowsum(dO * O) and lse * log2(e) in the padded [B*Hq, Npad] layout (D = 0 and
+// lse = +inf past N, which zeroes P for padded query rows); zeroes the dQ accumulator.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__ BwdParams p) {
+  constexpr int LPR = D / 8;  // lanes per row, 8 elements (16 B) per lane
+  const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, part = lane % LPR;
+  const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  for (long long base = wid * (32 / LPR); base < rows; base += warps_total * (32 / LPR)) {
+    const long long r = base + sub;
+    float acc = 0.f;
+    if (r < rows) {
+      const uint4 a = *reinterpret_cast<const uint4*>(p.o + r * D + part * 8);
+      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + r * D + part * 8);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        acc += bw_unpack_lo<BF16>(av[i]) * bw_unpack_lo<BF16>(gv[i]) +
+               bw_unpack_hi<BF16>(av[i]) * bw_unpack_hi<BF16>(gv[i]);
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + r * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (r < rows && part == 0) {
+      // r = (b*N + n)*Hq + h
+      const int h = static_cast<int>(r % p.Hq);
+      const long long bn = r / p.Hq;
+      const int n = static_cast<int>(bn % p.N);
+      const int b = static_cast<int>(bn / p.N);
+      const long long bh = static_cast<long long>(b) * p.Hq + h;
+      p.dvec[bh * p.Npad + n] = acc;
+      p.l2vec[bh * p.Npad + n] = p.lse[bh * p.N + n] * kLog2e;
+    }
+  }
+  // padding entries n in [N, Npad)
+  const int pad = p.Npad - p.N;
+  const long long npad = static_cast<long long>(p.B) * p.Hq * pad;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < npad;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long bh = i / pad;
+    const int n = p.N + static_cast<int>(i % pad);
+    p.dvec[bh * p.Npad + n] = 0.f;
+    p.l2vec[bh * p.Npad + n] = INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------ dQ convert
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                         long long n8, float scale) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 o;
+    o.x = bw_pack2<BF16>(a.x * scale, a.y * scale);
+    o.y = bw_pack2<BF16>(a.z * scale, a.w * scale);
+    o.z = bw_pack2<BF16>(b.x * scale, b.y * scale);
+    o.w = bw_pack2<BF16>(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = o;
+  }
+}
+
+// ------------------------------------------------------------------- main kernel
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  const uint32_t kv_full = bar(C::B_KV), sdp_full = bar(C::B_SDP), dp_free = bar(C::B_DPFREE);
+  const uint32_t dq_full = bar(C::B_DQFULL), dq_free = bar(C::B_DQFREE), acc_done = bar(C::B_ACC);
+  const uint32_t final_bar = bar(C::B_FINAL);
+  auto ds_ready = [&](int b) { return bar(C::B_DSREADY + b); };
+  auto ds_free = [&](int b) { return bar(C::B_DSFREE + b); };
+  auto st_full = [&](int s) { return bar(C::B_STFULL + s); };
+  auto st_empty = [&](int s) { return bar(C::B_STFULL + C::STG + s); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work decode: key block jb (ascending: for causal the heaviest first), then
+  // (batch, key/value head).
+  const int N = p.N;
+  const int nkb = (N + 127) / 128;
+  const int BH = p.B * p.Hkv;
+  const int jb = static_cast<int>(blockIdx.x / BH);
+  const int bhk = static_cast<int>(blockIdx.x % BH);
+  const int hkv = bhk % p.Hkv;
+  const int b = bhk / p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int nqb = (N + 63) / 64;
+  const int qb0 = CAUSAL ? 2 * jb : 0;
+  const int nq = nqb - qb0;      // query blocks per head
+  const int T = G * nq;          // steps of this CTA
+  const int k0 = 128 * jb;
+  (void)nkb;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    wg_fail[0] = wg_fail[1] = 0;
+    mbar_init(kv_full, 1);
+    mbar_init(sdp_full, 1);
+    mbar_init(dp_free, 128);
+    mbar_init(ds_ready(0), 128);
+    mbar_init(ds_ready(1), 128);
+    mbar_init(ds_free(0), 1);
+    mbar_init(ds_free(1), 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(final_bar, 1);
+    for (int s = 0; s < C::STG; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t lim = p.wait_limit_ns;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(p.err, kDevErrTimeout);
+  };
+
+  if (warp >= 8) {
+    setmaxnreg_dec<80>();
+    if (warp == 8 && lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
+      for (int ch = 0; ch < C::CHUNKS; ++ch) {
+        tma_load_4d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, k0, b);
+        tma_load_4d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, k0, b);
+      }
+      bool ok = true;
+      int it = 0;
+      for (; it < T; ++it) {
+        const int s = it % C::STG;
+        if (it >= C::STG && !mbar_wait(st_empty(s), ((it / C::STG) - 1) & 1, abort_flag, lim)) {
+          ok = false;
+          break;
+        }
+        const int hq = hkv * G + it / nq;
+        const int q0 = 64 * (qb0 + it % nq);
+        mbar_arrive_expect_tx(st_full(s), 2 * C::Q_TILE + 2 * 256);
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          tma_load_4d(sbase + C::OFF_Q + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_q, st_full(s), ch * 64, hq, q0, b);
+          tma_load_4d(sbase + C::OFF_DO + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_do, st_full(s), ch * 64, hq, q0,
+                      b);
+        }
+        const long long row = (static_cast<long long>(b) * p.Hq + hq) * p.Npad + q0;
+        bulk_load(sbase + C::OFF_LD + s * 512, p.l2vec + row, 256, st_full(s));
+        bulk_load(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row, 256, st_full(s));
+      }
+      if (!ok) {
+        fail();
+        for (int i = (it > C::STG ? it - C::STG : 0); i < it; ++i)
+          mbar_wait(st_full(i % C::STG), (i / C::STG) & 1, nullptr, lim);
+        mbar_wait(kv_full, 0, nullptr, lim);
+      }
+    } else if (warp == 9 && lane == 0) {
+      // --------------------------------------------------------------- MMA issuer
+      constexpr uint32_t bf = BF16 ? 1u : 0u;
+      constexpr uint32_t id_sdp = idesc_f16(128, 64, bf, 0, 0);  // S^T, dP^T: M=keys, N=queries
+      constexpr uint32_t id_grad = idesc_f16(128, D, bf, 0, 1);  // dV, dK: M=keys, N=d, B MN-major
+      constexpr uint32_t id_dq = idesc_f16(128, 64, bf, 1, 1);   // dQ^T: M=d (padded to 128), N=queries
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+      bool ok = mbar_wait(kv_full, 0, abort_flag, lim);
+      for (int it = 0; it <= T && ok; ++it) {
+        if (it < T) {
+          const int s = it % C::STG, bb = it & 1;
+          if (!mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE, sDO = sbase + C::OFF_DO + s * C::Q_TILE;
+          // S^T = K Q^T  (both K-major)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t oa = (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, ob = (kk / 4) * C::Q_CHUNK + (kk % 4) * 32;
+            mma_ss(tbase + C::T_S + 64u * bb, smem_desc_sw128(sK + oa, 16, 1024), smem_desc_sw128(sQ + ob, 16, 1024),
+                   id_sdp, kk > 0);
+          }
+          if (it > 0 && !mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t oa = (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, ob = (kk / 4) * C::Q_CHUNK + (kk % 4) * 32;
+            mma_ss(tbase + C::T_DP, smem_desc_sw128(sV + oa, 16, 1024), smem_desc_sw128(sDO + ob, 16, 1024), id_sdp,
+                   kk > 0);
+          }
+          mma_commit(sdp_full);
+        }
+        if (it > 0) {
+          const int i = it - 1, s = i % C::STG, bb = i & 1;
+          if (!mbar_wait(ds_ready(bb), (i >> 1) & 1, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE, sDO = sbase + C::OFF_DO + s * C::Q_TILE;
+          const uint32_t sDS = sbase + C::OFF_DS + bb * C::DS_TILE;
+          // dV += P^T dO   (P^T from TMEM; dO MN-major: queries x d)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tbase + C::T_DV, tbase + C::T_S + 64u * bb + 8u * kk,
+                   smem_desc_sw128(sDO + kk * 2048, C::Q_CHUNK, 1024), id_grad, (i > 0 || kk > 0));
+          // dK += dS^T Q   (dS^T K-major in shared memory; Q MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tbase + C::T_DK, smem_desc_sw128(sDS + kk * 32, 16, 1024),
+                   smem_desc_sw128(sQ + kk * 2048, C::Q_CHUNK, 1024), id_grad, (i > 0 || kk > 0));
+          if (i > 0 && !mbar_wait(dq_free, (i - 1) & 1, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dQ^T = K^T dS^T  (K^T: MN-major view of the K tile, d padded to 128 rows;
+          // dS^T: MN-major, queries contiguous)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase + C::T_DQ, smem_desc_sw128(sK + kk * 2048, C::KV_CHUNK, 1024),
+                   smem_desc_sw128(sDS + kk * 2048, 1024, 1024), id_dq, kk > 0);
+          mma_commit(dq_full);
+          mma_commit(st_empty(s));
+          mma_commit(ds_free(bb));
+        }
+      }
+      if (!ok) fail();
+      mma_commit(acc_done);
+      mma_commit(final_bar);
+      mbar_wait(final_bar, 0, nullptr, lim);
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<208>();  // 128 x 80 + 256 x 208 <= 384 x 168 (the launch allocation)
+    const int wg = warp >> 2;                        // 0: softmax / dS, 1: dQ reduction
+    const int r = (warp & 3) * 32 + lane;            // TMEM lane: key row (wg 0) or d index (wg 1)
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    bool ok = true;
+    if (wg == 0) {
+      // ------------------------------------------------------ P^T and dS^T
+      const float cl2 = p.scale_log2;
+      const int key = k0 + r;
+      for (int it = 0; it < T; ++it) {
+        const int s = it % C::STG, bb = it & 1;
+        const int q0 = 64 * (qb0 + it % nq);
+        if (!__all_sync(0xffffffffu, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim) &&
+                                         mbar_wait(sdp_full, it & 1, abort_flag, lim))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(tbase + lane_off + C::T_S + 64u * bb, sv);
+        tmem_ld32(tbase + lane_off + C::T_S + 64u * bb + 32u, sv + 32);
+        tmem_ld32(tbase + lane_off + C::T_DP, dpv);
+        tmem_ld32(tbase + lane_off + C::T_DP + 32u, dpv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dp_free);
+        const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_LD + s * 512);
+        const float* dv = l2 + 64;
+        const bool diag = CAUSAL && (q0 < k0 + 128);
+        float pf[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float pc = bw_ex2(fmaf(__uint_as_float(sv[c]), cl2, -l2[c]));
+          if (diag && key > q0 + c) pc = 0.f;
+          pf[c] = pc;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = bw_pack2<BF16>(pf[2 * i], pf[2 * i + 1]);
+        tmem_st32(tbase + lane_off + C::T_S + 64u * bb, pk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          pk[i] = bw_pack2<BF16>(pf[2 * i] * (__uint_as_float(dpv[2 * i]) - dv[2 * i]),
+                                 pf[2 * i + 1] * (__uint_as_float(dpv[2 * i + 1]) - dv[2 * i + 1]));
+        if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(ds_free(bb), ((it >> 1) - 1) & 1, abort_flag, lim))) {
+          ok = false;
+          break;
+        }
+        // dS^T row r -> 128-byte swizzled row of the [128 keys x 64 queries] tile
+        uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_ready(bb));
+      }
+    } else {
+      // ------------------------------------------- dQ^T -> fp32 accumulator
+      for (int it = 0; it < T; ++it) {
+        const int hq = hkv * G + it / nq;
+        const int q0 = 64 * (qb0 + it % nq);
+        if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, lim))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(tbase + lane_off + C::T_DQ, v);
+        tmem_ld32(tbase + lane_off + C::T_DQ + 32u, v + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_free);
+        if (r < D) {
+          float* dst = p.dq_acc + ((static_cast<long long>(b) * N + q0) * p.Hq + hq) * D + r;
+          const long long qstride = static_cast<long long>(p.Hq) * D;
+          const int qn = N - q0 < 64 ? N - q0 : 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < qn) atomicAdd(dst + c * qstride, __uint_as_float(v[c]));
+        }
+      }
+    }
+    // ---- epilogue: dV (warpgroup 0) and scale * dK (warpgroup 1) -> 16-bit rows
+    if (!ok) {
+      wg_fail[wg] = 1;
+      fail();
+    }
+    if (!mbar_wait(acc_done, 0, abort_flag, lim)) {
+      wg_fail[wg] = 1;
+      fail();
+    }
+    named_bar_sync_n(1 + wg, 128);
+    if (wg_fail[wg] == 0) {
+      tc_fence_after();
+      const int key = k0 + r;
+      uint16_t* out = (wg == 0 ? p.dv : p.dk) + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
+      const float mul = wg == 0 ? 1.0f : p.scale;
+      const uint32_t col = wg == 0 ? C::T_DV : C::T_DK;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + col + 32u * c, v);
+        tmem_wait_ld();
+        if (key < N) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 o;
+            o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+            o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+            o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+            o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+            *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
+  {
+    const long long want = (rows * (D / 8) + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * sms ? (want > 0 ? want : 1) : 8LL * sms);
+    fa_bwd_preprocess<D, BF16><<<grid, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = fa_bwd_main<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const long long grid = static_cast<long long>((p.N + 127) / 128) * p.B * p.Hkv;
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long n8 = rows * D / 8;
+    const long long want = (n8 + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+    fa_bwd_dq_convert<BF16><<<grid, 256, 0, stream>>>(p.dq_acc, p.dq, n8, p.scale);
+    return cudaGetLastError();
+  }
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {
+  const bool bf = dtype == FA_BF16;
+  if (d == 128) {
+    if (bf) return causal ? launch_bwd_t<128, true, true>(p, stream) : launch_bwd_t<128, true, false>(p, stream);
+    return causal ? launch_bwd_t<128, false, true>(p, stream) : launch_bwd_t<128, false, false>(p, stream);
+  }
+  if (bf) return causal ? launch_bwd_t<64, true, true>(p, stream) : launch_bwd_t<64, true, false>(p, stream);
+  return causal ? launch_bwd_t<64, false, true>(p, stream) : launch_bwd_t<64, false, false>(p, stream);
+}
+
+}  // namespace fa

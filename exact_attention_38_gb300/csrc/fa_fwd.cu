@@ -64,10 +64,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -324,7 +320,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       // every thread of the warpgroup reaches this barrier; afterwards wg_fail[t]
       // is read-only, so the branch below is uniform across the warpgroup
-      named_bar_sync(1 + t, 128);
+      named_bar_sync_n(1 + t, 128);
       if (wg_fail[t] == 0) {
         tc_fence_after();
         // ---- epilogue: O / l -> 16-bit -> swizzled staging (Q_t's buffer) -> TMA store
@@ -348,7 +344,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(3 + t, 128);
+        named_bar_sync_n(3 + t, 128);
         if (rit == 0) {
           for (int ch = 0; ch < C::CHUNKS; ++ch)
             tma_store_4d(&p.tm_o, smem_u32(stage + ch * C::CHUNK_BYTES), ch * 64, h, r0_of(t), b);

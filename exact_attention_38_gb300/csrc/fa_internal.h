@@ -32,8 +32,33 @@ struct FwdParams {
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
                      fa_dtype dtype);
 
+struct BwdParams {
+  CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
+  CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
+  const uint16_t* o;        // [B, N, Hq, d] (preprocess)
+  const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
+  const float* lse;         // [B, Hq, N]
+  uint16_t* dq;             // [B, N, Hq, d]
+  uint16_t* dk;             // [B, N, Hkv, d]
+  uint16_t* dv;             // [B, N, Hkv, d]
+  float* dq_acc;            // workspace: fp32 [B, N, Hq, d]
+  float* dvec;              // workspace: D = rowsum(dO*O), [B*Hq, Npad]
+  float* l2vec;             // workspace: lse * log2(e), [B*Hq, Npad] (+inf past N)
+  unsigned* err;
+  int B, Hq, Hkv, N, Npad;
+  float scale, scale_log2;
+  uint64_t wait_limit_ns;
+};
+
+// Workspace layout for the backward pass (all offsets 256-byte aligned).
+struct BwdWorkspace {
+  size_t dq_acc_off, dvec_off, l2vec_off, total;
+};
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d);
+
 unsigned* device_error_word();  // address of this device's error word (device memory)
 
 cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
 
 }  // namespace fa

@@ -18,6 +18,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Barrier over `nthreads` threads (a multiple of 32) with id 1..15 (0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync_n(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Register rebalancing between warpgroups (all warps of a warpgroup execute it).
 template <int R>
 __device__ __forceinline__ void setmaxnreg_inc() {

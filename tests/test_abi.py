@@ -89,7 +89,9 @@ def test_workspace_size(lib):
     lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 5
     B, Hq, N, d = 2, 4, 300, 128
     rows = B * Hq * N
-    want = ((rows * d * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    npad = (N + 63) // 64 * 64
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    want = up(rows * d * 4) + 2 * up(B * Hq * npad * 4)
     assert lib.fa_bwd_workspace_size(B, Hq, 2, N, d) == want
     assert lib.fa_bwd_workspace_size(B, Hq, 3, N, d) == 0
     assert lib.fa_bwd_workspace_size(B, Hq, 2, N, 80) == 0
