@@ -98,6 +98,20 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   return r == CUDA_SUCCESS;
 }
 
+bool encode_dq_acc_map(CUtensorMap* map, const float* base, int B, int N, int H, int d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4,
+                                 static_cast<cuuint64_t>(N) * H * d * 4};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 64, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -170,6 +184,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
   p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
+  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B, N, Hq, d)) return FA_ERR_CUDA;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

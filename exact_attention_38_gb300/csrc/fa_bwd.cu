@@ -55,7 +55,9 @@ struct BwdCfg {
   static constexpr int OFF_Q = 2 * KV_TILE;                    // [STG] Q tiles
   static constexpr int OFF_DO = OFF_Q + STG * Q_TILE;          // [STG] dO tiles
   static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles
-  static constexpr int OFF_LD = OFF_DS + 2 * DS_TILE;          // [STG][2][64] floats: lse*log2e, D
+  static constexpr int DQ_TILE = 64 * D * 4;                  // dQ staging, [64 queries][D] fp32
+  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;
+  static constexpr int OFF_LD = OFF_DQ + DQ_TILE;              // [STG][2][64] floats: lse*log2e, D
   static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 8 * NBARS + 64;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -195,13 +197,13 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work decode: key block jb (ascending: for causal the heaviest first), then
-  // (batch, key/value head).
+  // ---- work decode: key blocks of one (batch, key/value head) are consecutive CTAs
+  // (ascending, so with the causal mask the heaviest come first); the CTAs resident
+  // at any time then share a few heads' Q, dO and dQ accumulator through L2.
   const int N = p.N;
   const int nkb = (N + 127) / 128;
-  const int BH = p.B * p.Hkv;
-  const int jb = static_cast<int>(blockIdx.x / BH);
-  const int bhk = static_cast<int>(blockIdx.x % BH);
+  const int jb = static_cast<int>(blockIdx.x % nkb);
+  const int bhk = static_cast<int>(blockIdx.x / nkb);
   const int hkv = bhk % p.Hkv;
   const int b = bhk / p.Hkv;
   const int G = p.Hq / p.Hkv;
@@ -210,7 +212,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
   const int nq = nqb - qb0;      // query blocks per head
   const int T = G * nq;          // steps of this CTA
   const int k0 = 128 * jb;
-  (void)nkb;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -440,15 +441,23 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dq_free);
+        // stage [64 queries][D] fp32 in shared memory, then one TMA reduce-add into the
+        // accumulator (rows past N are clipped by the tensor map)
+        float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
+        if (r == 0) bulk_wait_group_read0();  // the previous reduce has read the staging tile
+        named_bar_sync_n(2, 128);
         if (r < D) {
-          float* dst = p.dq_acc + ((static_cast<long long>(b) * N + q0) * p.Hq + hq) * D + r;
-          const long long qstride = static_cast<long long>(p.Hq) * D;
-          const int qn = N - q0 < 64 ? N - q0 : 64;
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < qn) atomicAdd(dst + c * qstride, __uint_as_float(v[c]));
+          for (int c = 0; c < 64; ++c) stage[c * D + r] = __uint_as_float(v[c]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync_n(2, 128);
+        if (r == 0) {
+          tma_reduce_add_4d(&p.tm_dq, sbase + C::OFF_DQ, 0, hq, q0, b);
+          bulk_commit_group();
         }
       }
+      if (r == 0) bulk_wait_group0();
     }
     // ---- epilogue: dV (warpgroup 0) and scale * dK (warpgroup 1) -> 16-bit rows
     if (!ok) {
@@ -459,7 +468,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
       wg_fail[wg] = 1;
       fail();
     }
-    named_bar_sync_n(1 + wg, 128);
+    named_bar_sync_n(3 + wg, 128);
     if (wg_fail[wg] == 0) {
       tc_fence_after();
       const int key = k0 + r;

@@ -88,13 +88,22 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work decode: heaviest (largest query offset) tiles first; heads of a GQA
-  // group adjacent so their CTAs share K/V through L2.
+  // ---- work decode.  Without the mask every tile costs the same, and the query
+  // blocks of one (batch, head) are consecutive CTAs so the resident CTAs share a few
+  // heads' K/V through L2.  With the causal mask tiles are issued heaviest first
+  // (largest query offset) across all heads, which balances the last waves.
+  // Consecutive heads of a GQA group share K/V in both orders.
   const int N = p.N;
   const int nqb = (N + 255) / 256;
   const int BH = p.B * p.Hq;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  int qb, bh;
+  if (CAUSAL) {
+    qb = nqb - 1 - static_cast<int>(blockIdx.x / BH);
+    bh = static_cast<int>(blockIdx.x % BH);
+  } else {
+    qb = static_cast<int>(blockIdx.x % nqb);
+    bh = static_cast<int>(blockIdx.x / nqb);
+  }
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;
   const int hkv = h / (p.Hq / p.Hkv);

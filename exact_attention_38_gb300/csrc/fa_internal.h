@@ -35,6 +35,7 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
   CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
+  CUtensorMap tm_dq;        // fp32 dQ accumulator [B, N, Hq, d], box {d, 1, 64, 1}, no swizzle
   const uint16_t* o;        // [B, N, Hq, d] (preprocess)
   const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
   const float* lse;         // [B, Hq, N]
@@ -55,6 +56,9 @@ struct BwdWorkspace {
   size_t dq_acc_off, dvec_off, l2vec_off, total;
 };
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d);
+
+// 4-D map over the fp32 dQ accumulator [B, N, H, d], box = {d, 1, 64, 1}, no swizzle.
+bool encode_dq_acc_map(CUtensorMap* map, const float* base, int B, int N, int H, int d);
 
 unsigned* device_error_word();  // address of this device's error word (device memory)
 

@@ -88,7 +88,9 @@ def _row_lse(s):
 def attn_fwd_rows(q, k, v, causal, scale, b, h, rows):
     """O and lse for query rows ``rows`` of batch ``b``, query head ``h``.
 
-    Returns (o [len(rows), d], lse [len(rows)]).
+    With the causal mask a chunk of rows only reads keys up to its last row (the
+    probabilities of later keys are exactly zero).  Returns (o [len(rows), d],
+    lse [len(rows)]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     hkv = _kv_head(h, q.shape[2], k.shape[2])
@@ -98,10 +100,11 @@ def attn_fwd_rows(q, k, v, causal, scale, b, h, rows):
     lse = np.empty(rows.size)
     for c0 in range(0, rows.size, _ROW_CHUNK):
         r = rows[c0:c0 + _ROW_CHUNK]
-        s = _row_scores(q[b, r, h, :], kb, r, causal, scale)
+        kmax = int(r.max()) + 1 if causal else kb.shape[0]
+        s = _row_scores(q[b, r, h, :], kb[:kmax], r, causal, scale)
         l = _row_lse(s)
         p = np.exp(s - l[:, None])
-        o[c0:c0 + r.size] = p @ vb
+        o[c0:c0 + r.size] = p @ vb[:kmax]
         lse[c0:c0 + r.size] = l
     return o, lse
 
@@ -179,21 +182,22 @@ def attn_bwd_dq_rows(q, k, v, do, causal, scale, b, h, rows):
     out = np.empty((rows.size, q.shape[3]))
     for c0 in range(0, rows.size, _ROW_CHUNK):
         r = rows[c0:c0 + _ROW_CHUNK]
-        s = _row_scores(q[b, r, h, :], kb, r, causal, scale)
+        kmax = int(r.max()) + 1 if causal else kb.shape[0]
+        s = _row_scores(q[b, r, h, :], kb[:kmax], r, causal, scale)
         p = np.exp(s - _row_lse(s)[:, None])
         dob = do[b, r, h, :]
-        Di = np.sum(dob * (p @ vb), axis=1)
-        ds = p * (dob @ vb.T - Di[:, None])
-        out[c0:c0 + r.size] = scale * (ds @ kb)
+        Di = np.sum(dob * (p @ vb[:kmax]), axis=1)
+        ds = p * (dob @ vb[:kmax].T - Di[:, None])
+        out[c0:c0 + r.size] = scale * (ds @ kb[:kmax])
     return out
 
 
 def attn_bwd_kv_rows(q, k, v, do, causal, scale, b, hkv, key_rows):
     """dK and dV for key rows ``key_rows`` of (b, key/value head ``hkv``).
 
-    Column j of P and dS over *all* query rows of every query head in the group
-    is needed, so this walks every query row (cost ~2*N^2*d per query head).
-    Returns (dk [len, d], dv [len, d]).
+    Column j of P and dS over the query rows that see key j, for every query head
+    in the group, is needed: all rows without the mask (cost ~2*N^2*d per query
+    head), rows i >= min(key_rows) with it.  Returns (dk [len, d], dv [len, d]).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     N, Hq = q.shape[1], q.shape[2]
@@ -203,13 +207,15 @@ def attn_bwd_kv_rows(q, k, v, do, causal, scale, b, hkv, key_rows):
     key_rows = np.asarray(key_rows, dtype=np.int64)
     dk = np.zeros((key_rows.size, k.shape[3]))
     dv = np.zeros((key_rows.size, v.shape[3]))
+    first = int(key_rows.min()) if causal else 0
     for h in range(hkv * grp, (hkv + 1) * grp):
-        for c0 in range(0, N, _ROW_CHUNK):
+        for c0 in range(first, N, _ROW_CHUNK):
             r = np.arange(c0, min(N, c0 + _ROW_CHUNK))
-            s = _row_scores(q[b, r, h, :], kb, r, causal, scale)
+            kmax = max(int(r.max()), int(key_rows.max())) + 1 if causal else N
+            s = _row_scores(q[b, r, h, :], kb[:kmax], r, causal, scale)
             p = np.exp(s - _row_lse(s)[:, None])
             dob = do[b, r, h, :]
-            Di = np.sum(dob * (p @ vb), axis=1)
+            Di = np.sum(dob * (p @ vb[:kmax]), axis=1)
             pj = p[:, key_rows]
             dsj = pj * (dob @ vb[key_rows].T - Di[:, None])
             dv += pj.T @ dob
