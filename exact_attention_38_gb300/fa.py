@@ -41,6 +41,8 @@ def _load():
     lib.fa_fwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_check_device_error.argtypes = [vp]
@@ -69,6 +71,12 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, d
     """Mirror of the C ``fa_bwd``."""
     return lib.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
                       int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, stream) -> int:
+    """Mirror of the C ``fa_bwd_noalloc`` (fa_bwd on the library's own scratch array)."""
+    return lib.fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
+                              int(dtype), stream)
 
 
 def fa_bwd_workspace_size(B, Hq, Hkv, N, d) -> int:

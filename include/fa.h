@@ -101,6 +101,38 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_stream_t stream);
 
 /*
+ * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fa_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers such as plugins or engines
+ * that are handed only their input and output buffers, programs whose allocator is
+ * frozen after start-up, and real-time paths where an allocation's latency or failure
+ * is not acceptable.  They cannot provide fa_bwd's workspace.
+ *
+ * Arguments, layouts and results are those of fa_bwd, without the workspace: the
+ * call uses a FA_NOALLOC_SCRATCH_BYTES array that lives in the library.  That array is
+ * reserved on every GPU that loads the library's device code and is held until the
+ * process exits.  The call itself allocates nothing (no cudaMalloc, no allocating
+ * library routine).
+ *  - Sizes whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES return
+ *    FA_ERR_UNSUPPORTED before any CUDA call (for example B=1, Hq=16, d=128 fits up
+ *    to N of about 4000); other argument errors are fa_bwd's.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call outside
+ *    any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents; each call re-initialises what it reads (the dQ accumulator is zeroed,
+ *    D and lse are rewritten).  Calls that may overlap on the GPU (other streams,
+ *    other host threads) race on the array and give wrong results: serialise them.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                         int causal, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting and wound down without
  * finishing its work; its outputs are undefined) or FA_ERR_CUDA.
