@@ -106,8 +106,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ------------------------------------------------------------------- preprocess
-// D = rowsum(dO * O) and lse * log2(e) in the padded [B*Hq, Npad] layout (D = 0 and
-// lse = +inf past N, which zeroes P for padded query rows); zeroes the dQ accumulator.
+// -D = -rowsum(dO * O) and -lse * log2(e) in the padded [B*Hq, Npad] layout (negated so
+// the main kernel adds them; 0 and -inf past N, which zeroes P for padded query rows);
+// zeroes the dQ accumulator.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__ BwdParams p) {
   constexpr int LPR = D / 8;  // lanes per row, 8 elements (16 B) per lane
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
       const int n = static_cast<int>(bn % p.N);
       const int b = static_cast<int>(bn / p.N);
       const long long bh = static_cast<long long>(b) * p.Hq + h;
-      p.dvec[bh * p.Npad + n] = acc;
-      p.l2vec[bh * p.Npad + n] = p.lse[bh * p.N + n] * kLog2e;
+      p.dvec[bh * p.Npad + n] = -acc;
+      p.l2vec[bh * p.Npad + n] = -p.lse[bh * p.N + n] * kLog2e;
     }
   }
   // padding entries n in [N, Npad)
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
     const long long bh = i / pad;
     const int n = p.N + static_cast<int>(i % pad);
     p.dvec[bh * p.Npad + n] = 0.f;
-    p.l2vec[bh * p.Npad + n] = INFINITY;
+    p.l2vec[bh * p.Npad + n] = -INFINITY;
   }
 }
 
@@ -249,122 +250,149 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
 
   if (warp >= 8) {
     setmaxnreg_dec<80>();
-    if (warp == 8 && lane == 0) {
+    // The control warps run their loops with all 32 lanes (warp-uniform control flow,
+    // so loop state and descriptors live in uniform registers); one elected lane issues
+    // the copies, the tcgen05 instructions and their commits.
+    constexpr unsigned FULL = 0xffffffffu;
+    const bool leader = elect_one();
+    if (warp == 8) {
       // ------------------------------------------------------------ TMA producer
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_do);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
-      for (int ch = 0; ch < C::CHUNKS; ++ch) {
-        tma_load_4d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, k0, b);
-        tma_load_4d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, k0, b);
+      if (leader) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_do);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_dq);
+        mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          tma_load_4d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, k0, b);
+          tma_load_4d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, k0, b);
+        }
       }
       bool ok = true;
       int it = 0;
       for (; it < T; ++it) {
         const int s = it % C::STG;
-        if (it >= C::STG && !mbar_wait(st_empty(s), ((it / C::STG) - 1) & 1, abort_flag, lim)) {
+        if (it >= C::STG &&
+            !__all_sync(FULL, mbar_wait(st_empty(s), ((it / C::STG) - 1) & 1, abort_flag, lim))) {
           ok = false;
           break;
         }
         const int hq = hkv * G + it / nq;
         const int q0 = 64 * (qb0 + it % nq);
-        mbar_arrive_expect_tx(st_full(s), 2 * C::Q_TILE + 2 * 256);
-        for (int ch = 0; ch < C::CHUNKS; ++ch) {
-          tma_load_4d(sbase + C::OFF_Q + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_q, st_full(s), ch * 64, hq, q0, b);
-          tma_load_4d(sbase + C::OFF_DO + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_do, st_full(s), ch * 64, hq, q0,
-                      b);
+        if (leader) {
+          mbar_arrive_expect_tx(st_full(s), 2 * C::Q_TILE + 2 * 256);
+          for (int ch = 0; ch < C::CHUNKS; ++ch) {
+            tma_load_4d(sbase + C::OFF_Q + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_q, st_full(s), ch * 64, hq, q0,
+                        b);
+            tma_load_4d(sbase + C::OFF_DO + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_do, st_full(s), ch * 64, hq,
+                        q0, b);
+          }
+          const long long row = (static_cast<long long>(b) * p.Hq + hq) * p.Npad + q0;
+          bulk_load(sbase + C::OFF_LD + s * 512, p.l2vec + row, 256, st_full(s));
+          bulk_load(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row, 256, st_full(s));
         }
-        const long long row = (static_cast<long long>(b) * p.Hq + hq) * p.Npad + q0;
-        bulk_load(sbase + C::OFF_LD + s * 512, p.l2vec + row, 256, st_full(s));
-        bulk_load(sbase + C::OFF_LD + s * 512 + 256, p.dvec + row, 256, st_full(s));
       }
       if (!ok) {
-        fail();
+        if (leader) fail();
         for (int i = (it > C::STG ? it - C::STG : 0); i < it; ++i)
           mbar_wait(st_full(i % C::STG), (i / C::STG) & 1, nullptr, lim);
         mbar_wait(kv_full, 0, nullptr, lim);
       }
-    } else if (warp == 9 && lane == 0) {
+      __syncwarp();
+    } else if (warp == 9) {
       // --------------------------------------------------------------- MMA issuer
       constexpr uint32_t bf = BF16 ? 1u : 0u;
       constexpr uint32_t id_sdp = idesc_f16(128, 64, bf, 0, 0);  // S^T, dP^T: M=keys, N=queries
       constexpr uint32_t id_grad = idesc_f16(128, D, bf, 0, 1);  // dV, dK: M=keys, N=d, B MN-major
       constexpr uint32_t id_dq = idesc_f16(128, 64, bf, 1, 1);   // dQ^T: M=d (padded to 128), N=queries
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-      bool ok = mbar_wait(kv_full, 0, abort_flag, lim);
+      // descriptor templates; per step only the start-address field (16-byte units) moves
+      const uint64_t dK_km = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dV_km = smem_desc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t dQ_km = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dDO_km = smem_desc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dQ_mn = smem_desc_sw128(sbase + C::OFF_Q, C::Q_CHUNK, 1024);
+      const uint64_t dDO_mn = smem_desc_sw128(sbase + C::OFF_DO, C::Q_CHUNK, 1024);
+      const uint64_t dDS_km = smem_desc_sw128(sbase + C::OFF_DS, 16, 1024);
+      const uint64_t dDS_mn = smem_desc_sw128(sbase + C::OFF_DS, 1024, 1024);
+      const uint64_t dK_mn = smem_desc_sw128(sbase + C::OFF_K, C::KV_CHUNK, 1024);
+      auto u16 = [](int bytes) { return static_cast<uint64_t>(bytes >> 4); };
+      bool ok = __all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim));
       for (int it = 0; it <= T && ok; ++it) {
         if (it < T) {
           const int s = it % C::STG, bb = it & 1;
-          if (!mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim)) {
+          if (!__all_sync(FULL, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE, sDO = sbase + C::OFF_DO + s * C::Q_TILE;
+          const uint64_t qs = u16(s * C::Q_TILE);
           // S^T = K Q^T  (both K-major)
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t oa = (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, ob = (kk / 4) * C::Q_CHUNK + (kk % 4) * 32;
-            mma_ss(tbase + C::T_S + 64u * bb, smem_desc_sw128(sK + oa, 16, 1024), smem_desc_sw128(sQ + ob, 16, 1024),
-                   id_sdp, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tbase + C::T_S + 64u * bb, dK_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
+                     dQ_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
           }
-          if (it > 0 && !mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim)) {
+          if (it > 0 && !__all_sync(FULL, mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
           tc_fence_after();
           // dP^T = V dO^T
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t oa = (kk / 4) * C::KV_CHUNK + (kk % 4) * 32, ob = (kk / 4) * C::Q_CHUNK + (kk % 4) * 32;
-            mma_ss(tbase + C::T_DP, smem_desc_sw128(sV + oa, 16, 1024), smem_desc_sw128(sDO + ob, 16, 1024), id_sdp,
-                   kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tbase + C::T_DP, dV_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
+                     dDO_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
+            mma_commit(sdp_full);
           }
-          mma_commit(sdp_full);
         }
         if (it > 0) {
           const int i = it - 1, s = i % C::STG, bb = i & 1;
-          if (!mbar_wait(ds_ready(bb), (i >> 1) & 1, abort_flag, lim)) {
+          if (!__all_sync(FULL, mbar_wait(ds_ready(bb), (i >> 1) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE, sDO = sbase + C::OFF_DO + s * C::Q_TILE;
-          const uint32_t sDS = sbase + C::OFF_DS + bb * C::DS_TILE;
-          // dV += P^T dO   (P^T from TMEM; dO MN-major: queries x d)
+          const uint64_t qs = u16(s * C::Q_TILE), dss = u16(bb * C::DS_TILE);
+          if (leader) {
+            // dV += P^T dO   (P^T from TMEM; dO MN-major: queries x d)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tbase + C::T_DV, tbase + C::T_S + 64u * bb + 8u * kk,
-                   smem_desc_sw128(sDO + kk * 2048, C::Q_CHUNK, 1024), id_grad, (i > 0 || kk > 0));
-          // dK += dS^T Q   (dS^T K-major in shared memory; Q MN-major)
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tbase + C::T_DV, tbase + C::T_S + 64u * bb + 8u * kk, dDO_mn + qs + u16(kk * 2048), id_grad,
+                     (i > 0 || kk > 0));
+            // dK += dS^T Q   (dS^T K-major in shared memory; Q MN-major)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tbase + C::T_DK, smem_desc_sw128(sDS + kk * 32, 16, 1024),
-                   smem_desc_sw128(sQ + kk * 2048, C::Q_CHUNK, 1024), id_grad, (i > 0 || kk > 0));
-          if (i > 0 && !mbar_wait(dq_free, (i - 1) & 1, abort_flag, lim)) {
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tbase + C::T_DK, dDS_km + dss + u16(kk * 32), dQ_mn + qs + u16(kk * 2048), id_grad,
+                     (i > 0 || kk > 0));
+          }
+          if (i > 0 && !__all_sync(FULL, mbar_wait(dq_free, (i - 1) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // dQ^T = K^T dS^T  (K^T: MN-major view of the K tile, d padded to 128 rows;
-          // dS^T: MN-major, queries contiguous)
+          if (leader) {
+            // dQ^T = K^T dS^T  (K^T: MN-major view of the K tile, d padded to 128 rows;
+            // dS^T: MN-major, queries contiguous)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tbase + C::T_DQ, smem_desc_sw128(sK + kk * 2048, C::KV_CHUNK, 1024),
-                   smem_desc_sw128(sDS + kk * 2048, 1024, 1024), id_dq, kk > 0);
-          mma_commit(dq_full);
-          mma_commit(st_empty(s));
-          mma_commit(ds_free(bb));
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tbase + C::T_DQ, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq, kk > 0);
+            mma_commit(dq_full);
+            mma_commit(st_empty(s));
+            mma_commit(ds_free(bb));
+          }
         }
       }
-      if (!ok) fail();
-      mma_commit(acc_done);
-      mma_commit(final_bar);
+      if (!ok && leader) fail();
+      if (leader) {
+        mma_commit(acc_done);
+        mma_commit(final_bar);
+      }
       mbar_wait(final_bar, 0, nullptr, lim);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     setmaxnreg_inc<208>();  // 128 x 80 + 256 x 208 <= 384 x 168 (the launch allocation)
     const int wg = warp >> 2;                        // 0: softmax / dS, 1: dQ reduction
@@ -374,6 +402,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
     if (wg == 0) {
       // ------------------------------------------------------ P^T and dS^T
       const float cl2 = p.scale_log2;
+      const uint64_t cl2x2 = f2pack(cl2, cl2);
       const int key = k0 + r;
       for (int it = 0; it < T; ++it) {
         const int s = it % C::STG, bb = it & 1;
@@ -392,34 +421,63 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dp_free);
-        const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_LD + s * 512);
-        const float* dv = l2 + 64;
-        const bool diag = CAUSAL && (q0 < k0 + 128);
-        float pf[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float pc = bw_ex2(fmaf(__uint_as_float(sv[c]), cl2, -l2[c]));
-          if (diag && key > q0 + c) pc = 0.f;
-          pf[c] = pc;
-        }
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = bw_pack2<BF16>(pf[2 * i], pf[2 * i + 1]);
-        tmem_st32(tbase + lane_off + C::T_S + 64u * bb, pk);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          pk[i] = bw_pack2<BF16>(pf[2 * i] * (__uint_as_float(dpv[2 * i]) - dv[2 * i]),
-                                 pf[2 * i + 1] * (__uint_as_float(dpv[2 * i + 1]) - dv[2 * i + 1]));
+        // per query column: -lse*log2(e) and -D, staged by the producer (float4 loads, the
+        // same address in every lane)
+        const float4* nl4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512);
+        const float4* nd4 = nl4 + 16;
+        // with the causal mask query column c sees this key iff c >= key - q0
+        const int cmin = CAUSAL ? key - q0 : 0;
+        // the dS^T buffer of this parity must have been consumed by the MMAs of step it-2
         if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(ds_free(bb), ((it >> 1) - 1) & 1, abort_flag, lim))) {
           ok = false;
           break;
         }
         // dS^T row r -> 128-byte swizzled row of the [128 keys x 64 queries] tile
         uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
+        // 16 query columns at a time: P^T -> TMEM (8 packed columns), dS^T -> 2 x 16 B
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int g = 0; g < 4; ++g) {
+          uint32_t pk[8], dk2[8];
+#pragma unroll
+          for (int h4 = 0; h4 < 4; ++h4) {
+            const int c4 = 4 * g + h4;
+            const float4 L = nl4[c4], Dn = nd4[c4];
+            // x = s * scale*log2(e) - lse*log2(e), two columns per instruction
+            const uint64_t x01 = ffma2(f2pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])),
+                                       cl2x2, f2pack(L.x, L.y));
+            const uint64_t x23 = ffma2(f2pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])),
+                                       cl2x2, f2pack(L.z, L.w));
+            float p0, p1, p2, p3;
+            f2unpack(x01, p0, p1);
+            f2unpack(x23, p2, p3);
+            p0 = bw_ex2(p0);
+            p1 = bw_ex2(p1);
+            p2 = bw_ex2(p2);
+            p3 = bw_ex2(p3);
+            if (CAUSAL) {
+              if (4 * c4 + 0 < cmin) p0 = 0.f;
+              if (4 * c4 + 1 < cmin) p1 = 0.f;
+              if (4 * c4 + 2 < cmin) p2 = 0.f;
+              if (4 * c4 + 3 < cmin) p3 = 0.f;
+            }
+            // dS = P * (dP - D)
+            const uint64_t t01 = fadd2(f2pack(__uint_as_float(dpv[4 * c4]), __uint_as_float(dpv[4 * c4 + 1])),
+                                       f2pack(Dn.x, Dn.y));
+            const uint64_t t23 = fadd2(f2pack(__uint_as_float(dpv[4 * c4 + 2]), __uint_as_float(dpv[4 * c4 + 3])),
+                                       f2pack(Dn.z, Dn.w));
+            float d0, d1, d2, d3;
+            f2unpack(fmul2(f2pack(p0, p1), t01), d0, d1);
+            f2unpack(fmul2(f2pack(p2, p3), t23), d2, d3);
+            pk[2 * h4] = bw_pack2<BF16>(p0, p1);
+            pk[2 * h4 + 1] = bw_pack2<BF16>(p2, p3);
+            dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
+            dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
+          }
+          tmem_st8(tbase + lane_off + C::T_S + 64u * bb + 8u * g, pk);
+          *reinterpret_cast<uint4*>(rowp + (((2 * g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
+          *reinterpret_cast<uint4*>(rowp + (((2 * g + 1) ^ (r & 7)) * 16)) =
+              make_uint4(dk2[4], dk2[5], dk2[6], dk2[7]);
+        }
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();

@@ -145,10 +145,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 
   if (warp >= 8) {
    // control warpgroup gives registers to the softmax warpgroups
-   setmaxnreg_dec<56>();
+   setmaxnreg_dec<80>();
+   // The control warps run their loops with all 32 lanes (warp-uniform control flow,
+   // so loop state and descriptors live in uniform registers); one elected lane issues
+   // the TMA copies, the tcgen05 instructions and their commits.
+   constexpr unsigned FULL = 0xffffffffu;
+   const bool leader = elect_one();
    if (warp == 8) {
     // ------------------------------------------------------------- TMA producer
-    if (lane == 0) {
+    if (leader) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
@@ -160,15 +165,18 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
           tma_load_4d(smem_u32(sQ + t * C::TILE_BYTES + ch * C::CHUNK_BYTES), &p.tm_q, q_full(t), ch * 64, h,
                       r0_of(t), b);
       }
-      int c = 0;
-      bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
-        for (int kind = 0; kind < 2; ++kind, ++c) {
-          const int slot = c % C::STAGES;
-          if (c >= C::STAGES && !mbar_wait(kv_empty(slot), ((c / C::STAGES) - 1) & 1, abort_flag, lim)) {
-            ok = false;
-            break;
-          }
+    }
+    int c = 0;
+    bool ok = true;
+    for (int j = 0; j < nmax && ok; ++j) {
+      for (int kind = 0; kind < 2; ++kind, ++c) {
+        const int slot = c % C::STAGES;
+        if (c >= C::STAGES &&
+            !__all_sync(FULL, mbar_wait(kv_empty(slot), ((c / C::STAGES) - 1) & 1, abort_flag, lim))) {
+          ok = false;
+          break;
+        }
+        if (leader) {
           mbar_arrive_expect_tx(kv_full(slot), C::TILE_BYTES);
           const CUtensorMap* map = kind ? &p.tm_v : &p.tm_k;
           for (int ch = 0; ch < C::CHUNKS; ++ch)
@@ -176,81 +184,90 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                         hkv, 128 * j, b);
         }
       }
-      if (!ok) {
-        fail();
-        // let copies already in flight land before the CTA's shared memory goes away
-        for (int i = (c > C::STAGES ? c - C::STAGES : 0); i < c; ++i)
-          mbar_wait(kv_full(i % C::STAGES), (i / C::STAGES) & 1, no_abort, lim);
-        for (int t = 0; t < 2; ++t)
-          if (n_of(t)) mbar_wait(q_full(t), 0, no_abort, lim);
-      }
+    }
+    if (!ok) {
+      if (leader) fail();
+      // let copies already in flight land before the CTA's shared memory goes away
+      for (int i = (c > C::STAGES ? c - C::STAGES : 0); i < c; ++i)
+        mbar_wait(kv_full(i % C::STAGES), (i / C::STAGES) & 1, no_abort, lim);
+      for (int t = 0; t < 2; ++t)
+        if (n_of(t)) mbar_wait(q_full(t), 0, no_abort, lim);
     }
     __syncwarp();
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
-      constexpr uint32_t id_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (n_of(t)) ok = mbar_wait(q_full(t), 0, abort_flag, lim);
-      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
-      for (int j = 0; j <= nmax && ok; ++j) {
-        const int kc = 2 * j, vc = 2 * j - 1;
-        const int kslot = kc % C::STAGES, vslot = (vc + C::STAGES) % C::STAGES;
-        if (j < nmax && !mbar_wait(kv_full(kslot), (kc / C::STAGES) & 1, abort_flag, lim)) {
-          ok = false;
-          break;
-        }
-        if (j > 0 && !mbar_wait(kv_full(vslot), (vc / C::STAGES) & 1, abort_flag, lim)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t s_tm = tbase + 128u * t;
-          const uint32_t o_tm = tbase + 256u + uint32_t(D) * t;
-          if (j > 0 && j - 1 < n_of(t)) {
-            // O_t += P_t(j-1) V_{j-1}: P_t from TMEM (16-bit pairs over S_t), V MN-major.
-            if (!mbar_wait(p_full(t), (j - 1) & 1, abort_flag, lim)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t vbase = skv + vslot * C::TILE_BYTES;
-            // MN-major operand: leading-dimension offset = stride between 64-column
-            // chunks, stride-dimension offset = stride between 8-key row groups.
+    constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+    constexpr uint32_t id_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+    bool ok = true;
+    for (int t = 0; t < 2 && ok; ++t)
+      if (n_of(t)) ok = __all_sync(FULL, mbar_wait(q_full(t), 0, abort_flag, lim));
+    const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
+    // descriptor templates; per k-step only the start-address field (bits 0-13, in
+    // 16-byte units) moves, and it never carries out of its field inside the CTA's
+    // shared memory window
+    const uint64_t dq0 = smem_desc_sw128(sq, 16, 1024), dkv0 = smem_desc_sw128(skv, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(skv, C::CHUNK_BYTES, 1024);
+    for (int j = 0; j <= nmax && ok; ++j) {
+      const int kc = 2 * j, vc = 2 * j - 1;
+      const int kslot = kc % C::STAGES, vslot = (vc + C::STAGES) % C::STAGES;
+      if (j < nmax && !__all_sync(FULL, mbar_wait(kv_full(kslot), (kc / C::STAGES) & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      if (j > 0 && !__all_sync(FULL, mbar_wait(kv_full(vslot), (vc / C::STAGES) & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t s_tm = tbase + 128u * t;
+        const uint32_t o_tm = tbase + 256u + uint32_t(D) * t;
+        if (j > 0 && j - 1 < n_of(t)) {
+          // O_t += P_t(j-1) V_{j-1}: P_t from TMEM (16-bit pairs over S_t), V MN-major.
+          if (!__all_sync(FULL, mbar_wait(p_full(t), (j - 1) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // MN-major operand: leading-dimension offset = stride between 64-column
+          // chunks, stride-dimension offset = stride between 8-key row groups.
+          const uint64_t vd = dv0 + static_cast<uint64_t>((vslot * C::TILE_BYTES) >> 4);
+          if (leader) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ts(o_tm, s_tm + 8u * kk, smem_desc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), id_pv,
+              mma_ts(o_tm, s_tm + 8u * kk, vd + static_cast<uint64_t>((kk * 2048) >> 4), id_pv,
                      (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == n_of(t) - 1) mma_commit(o_done(t));
           }
-          if (j < n_of(t)) {
-            // S_t = Q_t K_j^T, both K-major.
-            const uint32_t qbase = sq + t * C::TILE_BYTES, kbase = skv + kslot * C::TILE_BYTES;
+        }
+        if (j < n_of(t)) {
+          // S_t = Q_t K_j^T, both K-major.
+          const uint64_t qd = dq0 + static_cast<uint64_t>((t * C::TILE_BYTES) >> 4);
+          const uint64_t kd = dkv0 + static_cast<uint64_t>((kslot * C::TILE_BYTES) >> 4);
+          if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
-              mma_ss(s_tm, smem_desc_sw128(qbase + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024), id_qk,
-                     kk > 0 ? 1u : 0u);
+              const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4);
+              mma_ss(s_tm, qd + off, kd + off, id_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(s_full(t));
           }
         }
-        if (!ok) break;
+      }
+      if (!ok) break;
+      if (leader) {
         if (j > 0) mma_commit(kv_empty(vslot));
         if (j < nmax) mma_commit(kv_empty(kslot));
       }
-      if (!ok) fail();
-      // every MMA this thread issued must be finished before TMEM is released
-      mma_commit(final_bar);
-      mbar_wait(final_bar, 0, no_abort, lim);
     }
+    if (!ok && leader) fail();
+    // every MMA the leader issued must be finished before TMEM is released
+    if (leader) mma_commit(final_bar);
+    mbar_wait(final_bar, 0, no_abort, lim);
     __syncwarp();
    }
   } else {
-    setmaxnreg_inc<224>();
+    setmaxnreg_inc<208>();
     // ----------------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;
     const int rit = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
@@ -274,12 +291,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       tmem_wait_ld();
       float* s = reinterpret_cast<float*>(sr);
       if (j == n_of(t) - 1 && (CAUSAL || (N & 127))) {
+        // keys k0 + c are visible for c < nvis (key < N, and key <= row with the mask)
         const int k0 = 128 * j;
+        const int nvis = CAUSAL ? min(N, row + 1) - k0 : N - k0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = k0 + c;
-          if (key >= N || (CAUSAL && key > row)) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c >= nvis) s[c] = -INFINITY;
       }
       float mx = s[0];
 #pragma unroll

@@ -43,8 +43,8 @@ struct BwdParams {
   uint16_t* dk;             // [B, N, Hkv, d]
   uint16_t* dv;             // [B, N, Hkv, d]
   float* dq_acc;            // workspace: fp32 [B, N, Hq, d]
-  float* dvec;              // workspace: D = rowsum(dO*O), [B*Hq, Npad]
-  float* l2vec;             // workspace: lse * log2(e), [B*Hq, Npad] (+inf past N)
+  float* dvec;              // workspace: -D = -rowsum(dO*O), [B*Hq, Npad] (0 past N)
+  float* l2vec;             // workspace: -lse * log2(e), [B*Hq, Npad] (-inf past N)
   unsigned* err;
   int B, Hq, Hkv, N, Npad;
   float scale, scale_log2;
