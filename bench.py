@@ -76,6 +76,25 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+# ------------------------------------------------------- multi-rank aggregation
+
+def reduce_step_time(ms_local, world, device=None):
+    """Max over ranks of the per-step time (every rank runs its own replica)."""
+    if world <= 1:
+        return float(ms_local)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step, world, ms_step):
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------- clocks during timing
 
 class ClockSampler:
@@ -249,14 +268,11 @@ def run_native(a):
         t_wall = time.perf_counter() - t_wall
     fa.check_device_error()
     per = {n: [e0.elapsed_time(e1) for e0, e1 in ev[n]] for n in ev}
-    ms_step = sum(statistics.mean(per[n]) for n in per)
-    t_max = torch.tensor([ms_step], device=dev)
+    ms_step = reduce_step_time(sum(statistics.mean(per[n]) for n in per), world, dev)
     if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
         dist.barrier()
-    ms_step = float(t_max.item())
     fl_step = flops(w, a.which)
-    value = world * fl_step / (ms_step * 1e-3) / 1e12
+    value = job_throughput(fl_step, world, ms_step)
 
     # ---- e2e: host buffers through the C ABI, copies inside the timed region
     e2e = None
@@ -283,12 +299,9 @@ def run_native(a):
                     h_.copy_(d_, non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / K
-        t2 = torch.tensor([ms_e2e], device=dev)
-        if world > 1:
-            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * fl_step / (float(t2.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(t2.item())}
+        ms_e2e = reduce_step_time(e0.elapsed_time(e1) / K, world, dev)
+        e2e = {"value": job_throughput(fl_step, world, ms_e2e), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
         fa.check_device_error()
 
     if rank != 0:

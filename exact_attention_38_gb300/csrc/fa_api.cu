@@ -58,11 +58,10 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int dty
 
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t rows = static_cast<size_t>(B) * N * Hq;
   const size_t npad = (static_cast<size_t>(N) + 63) / 64 * 64;
   BwdWorkspace w{};
   w.dq_acc_off = 0;
-  w.dvec_off = up(rows * d * 4);
+  w.dvec_off = up(static_cast<size_t>(B) * Hq * d * npad * 4);
   w.l2vec_off = w.dvec_off + up(static_cast<size_t>(B) * Hq * npad * 4);
   w.total = w.l2vec_off + up(static_cast<size_t>(B) * Hq * npad * 4);
   return w;
@@ -98,17 +97,15 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   return r == CUDA_SUCCESS;
 }
 
-bool encode_dq_acc_map(CUtensorMap* map, const float* base, int B, int N, int H, int d) {
+bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, int d) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4,
-                                 static_cast<cuuint64_t>(N) * H * d * 4};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 64, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Npad), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Npad) * 4, static_cast<cuuint64_t>(d) * Npad * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(d), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -184,7 +181,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
   p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
-  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B, N, Hq, d)) return FA_ERR_CUDA;
+  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d)) return FA_ERR_CUDA;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

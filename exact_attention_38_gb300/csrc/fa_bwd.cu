@@ -18,12 +18,13 @@
 // fa_bwd_main: one CTA per (batch, key/value head, block of 128 keys).  K_j and V_j stay
 // in shared memory; the CTA walks every query head of its GQA group and every visible
 // block of 64 queries.  Per step the tensor cores compute S^T = K Q^T and dP^T = V dO^T
-// into tensor memory (S^T double-buffered), a softmax warpgroup (thread = key row =
-// TMEM lane) turns them into P^T (written back to TMEM as 16-bit pairs) and dS^T
-// (written to swizzled shared memory), and the tensor cores then accumulate
-// dV += P^T dO and dK += dS^T Q in TMEM for the whole walk and compute
-// dQ^T = K^T dS^T, which a second warpgroup adds into the fp32 dQ accumulator with
-// coalesced reductions while the next step's S^T / dP^T run.
+// into tensor memory (S^T double-buffered); two softmax warpgroups (thread = key row =
+// TMEM lane, each taking 32 of the 64 query columns) turn them into P^T (written back
+// to TMEM as 16-bit pairs) and dS^T (written to swizzled shared memory); the tensor
+// cores then accumulate dV += P^T dO and dK += dS^T Q in TMEM for the whole walk and
+// compute dQ^T = K^T dS^T, which a fourth warpgroup stages in shared memory and adds
+// into the fp32 dQ accumulator with TMA bulk tensor reductions while the next step's
+// S^T / dP^T run.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -43,8 +44,9 @@ struct BwdCfg {
   static constexpr int Q_CHUNK = 64 * 128;        // 64 rows x 128 B
   static constexpr int Q_TILE = 64 * D * 2;       // Q or dO tile
   static constexpr int DS_TILE = 128 * 64 * 2;    // dS^T tile, 128 keys x 64 queries, 16-bit
+  static constexpr int DQ_HALF = D * 128;         // dQ^T staging: D rows x 32 fp32 queries (128 B)
   static constexpr int STG = (D == 128) ? 3 : 5;  // Q/dO/lse/D stages
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
   // barrier indices
   static constexpr int B_KV = 0, B_SDP = 1, B_DPFREE = 2, B_DSREADY = 3 /*[2]*/, B_DSFREE = 5 /*[2]*/,
                        B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_STFULL = 11 /*[STG]*/;
@@ -55,9 +57,8 @@ struct BwdCfg {
   static constexpr int OFF_Q = 2 * KV_TILE;                    // [STG] Q tiles
   static constexpr int OFF_DO = OFF_Q + STG * Q_TILE;          // [STG] dO tiles
   static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles
-  static constexpr int DQ_TILE = 64 * D * 4;                  // dQ staging, [64 queries][D] fp32
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;
-  static constexpr int OFF_LD = OFF_DQ + DQ_TILE;              // [STG][2][64] floats: lse*log2e, D
+  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;          // [2] dQ^T staging halves
+  static constexpr int OFF_LD = OFF_DQ + 2 * DQ_HALF;          // [STG][2][64] floats: -lse*log2e, -D
   static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 8 * NBARS + 64;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -108,7 +109,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // ------------------------------------------------------------------- preprocess
 // -D = -rowsum(dO * O) and -lse * log2(e) in the padded [B*Hq, Npad] layout (negated so
 // the main kernel adds them; 0 and -inf past N, which zeroes P for padded query rows);
-// zeroes the dQ accumulator.
+// zeroes the dQ accumulator ([B*Hq, d, Npad] fp32).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__ BwdParams p) {
   constexpr int LPR = D / 8;  // lanes per row, 8 elements (16 B) per lane
@@ -128,9 +129,6 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
       for (int i = 0; i < 4; ++i)
         acc += bw_unpack_lo<BF16>(av[i]) * bw_unpack_lo<BF16>(gv[i]) +
                bw_unpack_hi<BF16>(av[i]) * bw_unpack_hi<BF16>(gv[i]);
-      float4* z = reinterpret_cast<float4*>(p.dq_acc + r * D + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -145,45 +143,62 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
       p.l2vec[bh * p.Npad + n] = -p.lse[bh * p.N + n] * kLog2e;
     }
   }
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   // padding entries n in [N, Npad)
   const int pad = p.Npad - p.N;
   const long long npad = static_cast<long long>(p.B) * p.Hq * pad;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < npad;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+  for (long long i = tid; i < npad; i += nthreads) {
     const long long bh = i / pad;
     const int n = p.N + static_cast<int>(i % pad);
     p.dvec[bh * p.Npad + n] = 0.f;
     p.l2vec[bh * p.Npad + n] = -INFINITY;
   }
+  // dQ accumulator = 0 (16 B per thread per step)
+  const long long nacc4 = static_cast<long long>(p.B) * p.Hq * D * p.Npad / 4;
+  float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+  for (long long i = tid; i < nacc4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ dQ convert
-template <bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                         long long n8, float scale) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+// dQ[b, n, h, :] = scale * acc[b*Hq + h, :, n]: a tiled transpose through shared memory
+// (coalesced fp32 reads along n, coalesced 16-bit writes along d).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__ BwdParams p) {
+  __shared__ float tile[D][65];
+  const int nblk = (p.N + 63) / 64;
+  const int bh = static_cast<int>(blockIdx.x / nblk);
+  const int n0 = 64 * static_cast<int>(blockIdx.x % nblk);
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const float* src = p.dq_acc + static_cast<long long>(bh) * D * p.Npad + n0;
+  for (int i = threadIdx.x; i < D * 64; i += 256) {
+    const int dd = i >> 6, n = i & 63;
+    tile[dd][n] = src[static_cast<long long>(dd) * p.Npad + n];
+  }
+  __syncthreads();
+  constexpr int G = D / 8;  // 8 outputs (16 B) per thread and step
+  for (int i = threadIdx.x; i < 64 * G; i += 256) {
+    const int n = i / G, g = i % G;
+    if (n0 + n >= p.N) continue;
     uint4 o;
-    o.x = bw_pack2<BF16>(a.x * scale, a.y * scale);
-    o.y = bw_pack2<BF16>(a.z * scale, a.w * scale);
-    o.z = bw_pack2<BF16>(b.x * scale, b.y * scale);
-    o.w = bw_pack2<BF16>(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4*>(dq)[i] = o;
+    o.x = bw_pack2<BF16>(tile[8 * g + 0][n] * p.scale, tile[8 * g + 1][n] * p.scale);
+    o.y = bw_pack2<BF16>(tile[8 * g + 2][n] * p.scale, tile[8 * g + 3][n] * p.scale);
+    o.z = bw_pack2<BF16>(tile[8 * g + 4][n] * p.scale, tile[8 * g + 5][n] * p.scale);
+    o.w = bw_pack2<BF16>(tile[8 * g + 6][n] * p.scale, tile[8 * g + 7][n] * p.scale);
+    *reinterpret_cast<uint4*>(p.dq + ((static_cast<long long>(b) * p.N + n0 + n) * p.Hq + h) * D + 8 * g) = o;
   }
 }
 
 // ------------------------------------------------------------------- main kernel
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [4]
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * i; };
@@ -194,6 +209,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
   auto ds_free = [&](int b) { return bar(C::B_DSFREE + b); };
   auto st_full = [&](int s) { return bar(C::B_STFULL + s); };
   auto st_empty = [&](int s) { return bar(C::B_STFULL + C::STG + s); };
+  constexpr unsigned FULL = 0xffffffffu;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -216,12 +232,12 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    wg_fail[0] = wg_fail[1] = 0;
+    wg_fail[0] = wg_fail[1] = wg_fail[2] = wg_fail[3] = 0;
     mbar_init(kv_full, 1);
     mbar_init(sdp_full, 1);
-    mbar_init(dp_free, 128);
-    mbar_init(ds_ready(0), 128);
-    mbar_init(ds_ready(1), 128);
+    mbar_init(dp_free, 256);
+    mbar_init(ds_ready(0), 256);
+    mbar_init(ds_ready(1), 256);
     mbar_init(ds_free(0), 1);
     mbar_init(ds_free(1), 1);
     mbar_init(dq_full, 1);
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
     }
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -247,15 +263,18 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
     *abort_flag = 1;
     atomicOr(p.err, kDevErrTimeout);
   };
+  const int wg = warp >> 2;                        // 0,1: softmax; 2: dQ; 3: control
+  const int r = (warp & 3) * 32 + lane;            // TMEM lane: key row (wg 0,1) or d index (wg 2)
+  const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
 
-  if (warp >= 8) {
+  if (wg == 3) {
+    // launch allocation 512 x 128 registers: control 80, dQ 112, softmax 2 x 160
     setmaxnreg_dec<80>();
     // The control warps run their loops with all 32 lanes (warp-uniform control flow,
     // so loop state and descriptors live in uniform registers); one elected lane issues
     // the copies, the tcgen05 instructions and their commits.
-    constexpr unsigned FULL = 0xffffffffu;
     const bool leader = elect_one();
-    if (warp == 8) {
+    if (warp == 12) {
       // ------------------------------------------------------------ TMA producer
       if (leader) {
         tma_prefetch_desc(&p.tm_q);
@@ -300,7 +319,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
         mbar_wait(kv_full, 0, nullptr, lim);
       }
       __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
       // --------------------------------------------------------------- MMA issuer
       constexpr uint32_t bf = BF16 ? 1u : 0u;
       constexpr uint32_t id_sdp = idesc_f16(128, 64, bf, 0, 0);  // S^T, dP^T: M=keys, N=queries
@@ -367,6 +386,8 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tbase + C::T_DK, dDS_km + dss + u16(kk * 32), dQ_mn + qs + u16(kk * 2048), id_grad,
                      (i > 0 || kk > 0));
+            // the stage's Q / dO are no longer read once these complete
+            mma_commit(st_empty(s));
           }
           if (i > 0 && !__all_sync(FULL, mbar_wait(dq_free, (i - 1) & 1, abort_flag, lim))) {
             ok = false;
@@ -380,7 +401,6 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tbase + C::T_DQ, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq, kk > 0);
             mma_commit(dq_full);
-            mma_commit(st_empty(s));
             mma_commit(ds_free(bb));
           }
         }
@@ -393,159 +413,195 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
       mbar_wait(final_bar, 0, nullptr, lim);
       __syncwarp();
     }
-  } else {
-    setmaxnreg_inc<208>();  // 128 x 80 + 256 x 208 <= 384 x 168 (the launch allocation)
-    const int wg = warp >> 2;                        // 0: softmax / dS, 1: dQ reduction
-    const int r = (warp & 3) * 32 + lane;            // TMEM lane: key row (wg 0) or d index (wg 1)
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+  } else if (wg < 2) {
+    setmaxnreg_inc<160>();
+    // ------------------------------------------------------ P^T and dS^T
+    // warpgroup wg takes query columns [32 wg, 32 wg + 32) of each 64-column step
     bool ok = true;
-    if (wg == 0) {
-      // ------------------------------------------------------ P^T and dS^T
-      const float cl2 = p.scale_log2;
-      const uint64_t cl2x2 = f2pack(cl2, cl2);
-      const int key = k0 + r;
-      for (int it = 0; it < T; ++it) {
-        const int s = it % C::STG, bb = it & 1;
-        const int q0 = 64 * (qb0 + it % nq);
-        if (!__all_sync(0xffffffffu, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim) &&
-                                         mbar_wait(sdp_full, it & 1, abort_flag, lim))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(tbase + lane_off + C::T_S + 64u * bb, sv);
-        tmem_ld32(tbase + lane_off + C::T_S + 64u * bb + 32u, sv + 32);
-        tmem_ld32(tbase + lane_off + C::T_DP, dpv);
-        tmem_ld32(tbase + lane_off + C::T_DP + 32u, dpv + 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dp_free);
-        // per query column: -lse*log2(e) and -D, staged by the producer (float4 loads, the
-        // same address in every lane)
-        const float4* nl4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512);
-        const float4* nd4 = nl4 + 16;
-        // with the causal mask query column c sees this key iff c >= key - q0
-        const int cmin = CAUSAL ? key - q0 : 0;
-        // the dS^T buffer of this parity must have been consumed by the MMAs of step it-2
-        if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(ds_free(bb), ((it >> 1) - 1) & 1, abort_flag, lim))) {
-          ok = false;
-          break;
-        }
-        // dS^T row r -> 128-byte swizzled row of the [128 keys x 64 queries] tile
-        uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
-        // 16 query columns at a time: P^T -> TMEM (8 packed columns), dS^T -> 2 x 16 B
+    const float cl2 = p.scale_log2;
+    const uint64_t cl2x2 = f2pack(cl2, cl2);
+    const int key = k0 + r;
+    const int cbase = 32 * wg;
+    for (int it = 0; it < T; ++it) {
+      const int s = it % C::STG, bb = it & 1;
+      const int q0 = 64 * (qb0 + it % nq);
+      if (!__all_sync(FULL, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim) &&
+                                mbar_wait(sdp_full, it & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[32], dpv[32];
+      tmem_ld32(tbase + lane_off + C::T_S + 64u * bb + cbase, sv);
+      tmem_ld32(tbase + lane_off + C::T_DP + cbase, dpv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dp_free);
+      // per query column: -lse*log2(e) and -D, staged by the producer (float4 loads, the
+      // same address in every lane)
+      const float4* nl4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512) + cbase / 4;
+      const float4* nd4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512 + 256) + cbase / 4;
+      // with the causal mask query column c sees this key iff c >= key - q0
+      const int cmin = CAUSAL ? key - q0 - cbase : 0;
+      // the dS^T buffer of this parity must have been consumed by the MMAs of step it-2
+      if (it >= 2 && !__all_sync(FULL, mbar_wait(ds_free(bb), ((it >> 1) - 1) & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      // dS^T row r -> 128-byte swizzled row of the [128 keys x 64 queries] tile; this
+      // warpgroup writes 16-byte units [4 wg, 4 wg + 4)
+      uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
+      uint32_t pk[16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t pk[8], dk2[8];
+      for (int g = 0; g < 4; ++g) {
+        uint32_t dk2[4];
 #pragma unroll
-          for (int h4 = 0; h4 < 4; ++h4) {
-            const int c4 = 4 * g + h4;
-            const float4 L = nl4[c4], Dn = nd4[c4];
-            // x = s * scale*log2(e) - lse*log2(e), two columns per instruction
-            const uint64_t x01 = ffma2(f2pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])),
-                                       cl2x2, f2pack(L.x, L.y));
-            const uint64_t x23 = ffma2(f2pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])),
-                                       cl2x2, f2pack(L.z, L.w));
-            float p0, p1, p2, p3;
-            f2unpack(x01, p0, p1);
-            f2unpack(x23, p2, p3);
-            p0 = bw_ex2(p0);
-            p1 = bw_ex2(p1);
-            p2 = bw_ex2(p2);
-            p3 = bw_ex2(p3);
-            if (CAUSAL) {
-              if (4 * c4 + 0 < cmin) p0 = 0.f;
-              if (4 * c4 + 1 < cmin) p1 = 0.f;
-              if (4 * c4 + 2 < cmin) p2 = 0.f;
-              if (4 * c4 + 3 < cmin) p3 = 0.f;
-            }
-            // dS = P * (dP - D)
-            const uint64_t t01 = fadd2(f2pack(__uint_as_float(dpv[4 * c4]), __uint_as_float(dpv[4 * c4 + 1])),
-                                       f2pack(Dn.x, Dn.y));
-            const uint64_t t23 = fadd2(f2pack(__uint_as_float(dpv[4 * c4 + 2]), __uint_as_float(dpv[4 * c4 + 3])),
-                                       f2pack(Dn.z, Dn.w));
-            float d0, d1, d2, d3;
-            f2unpack(fmul2(f2pack(p0, p1), t01), d0, d1);
-            f2unpack(fmul2(f2pack(p2, p3), t23), d2, d3);
-            pk[2 * h4] = bw_pack2<BF16>(p0, p1);
-            pk[2 * h4 + 1] = bw_pack2<BF16>(p2, p3);
-            dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
-            dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
+        for (int h4 = 0; h4 < 2; ++h4) {
+          const int c4 = 2 * g + h4;
+          const float4 L = nl4[c4], Dn = nd4[c4];
+          // x = s * scale*log2(e) - lse*log2(e), two columns per instruction
+          const uint64_t x01 = ffma2(f2pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), cl2x2,
+                                     f2pack(L.x, L.y));
+          const uint64_t x23 = ffma2(f2pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])),
+                                     cl2x2, f2pack(L.z, L.w));
+          float p0, p1, p2, p3;
+          f2unpack(x01, p0, p1);
+          f2unpack(x23, p2, p3);
+          p0 = bw_ex2(p0);
+          p1 = bw_ex2(p1);
+          p2 = bw_ex2(p2);
+          p3 = bw_ex2(p3);
+          if (CAUSAL) {
+            if (4 * c4 + 0 < cmin) p0 = 0.f;
+            if (4 * c4 + 1 < cmin) p1 = 0.f;
+            if (4 * c4 + 2 < cmin) p2 = 0.f;
+            if (4 * c4 + 3 < cmin) p3 = 0.f;
           }
-          tmem_st8(tbase + lane_off + C::T_S + 64u * bb + 8u * g, pk);
-          *reinterpret_cast<uint4*>(rowp + (((2 * g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
-          *reinterpret_cast<uint4*>(rowp + (((2 * g + 1) ^ (r & 7)) * 16)) =
-              make_uint4(dk2[4], dk2[5], dk2[6], dk2[7]);
+          // dS = P * (dP - D)
+          const uint64_t t01 = fadd2(f2pack(__uint_as_float(dpv[4 * c4]), __uint_as_float(dpv[4 * c4 + 1])),
+                                     f2pack(Dn.x, Dn.y));
+          const uint64_t t23 = fadd2(f2pack(__uint_as_float(dpv[4 * c4 + 2]), __uint_as_float(dpv[4 * c4 + 3])),
+                                     f2pack(Dn.z, Dn.w));
+          float d0, d1, d2, d3;
+          f2unpack(fmul2(f2pack(p0, p1), t01), d0, d1);
+          f2unpack(fmul2(f2pack(p2, p3), t23), d2, d3);
+          pk[2 * c4] = bw_pack2<BF16>(p0, p1);
+          pk[2 * c4 + 1] = bw_pack2<BF16>(p2, p3);
+          dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
+          dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
         }
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(ds_ready(bb));
+        *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
       }
-    } else {
-      // ------------------------------------------- dQ^T -> fp32 accumulator
-      for (int it = 0; it < T; ++it) {
-        const int hq = hkv * G + it / nq;
-        const int q0 = 64 * (qb0 + it % nq);
-        if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, lim))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t v[64];
-        tmem_ld32(tbase + lane_off + C::T_DQ, v);
-        tmem_ld32(tbase + lane_off + C::T_DQ + 32u, v + 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_free);
-        // stage [64 queries][D] fp32 in shared memory, then one TMA reduce-add into the
-        // accumulator (rows past N are clipped by the tensor map)
-        float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
-        if (r == 0) bulk_wait_group_read0();  // the previous reduce has read the staging tile
-        named_bar_sync_n(2, 128);
-        if (r < D) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) stage[c * D + r] = __uint_as_float(v[c]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync_n(2, 128);
-        if (r == 0) {
-          tma_reduce_add_4d(&p.tm_dq, sbase + C::OFF_DQ, 0, hq, q0, b);
-          bulk_commit_group();
-        }
-      }
-      if (r == 0) bulk_wait_group0();
+      // P^T: 32 queries -> 16 packed columns at [16 wg, 16 wg + 16) of S^T's buffer
+      tmem_st16(tbase + lane_off + C::T_S + 64u * bb + 16u * wg, pk);
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_ready(bb));
     }
-    // ---- epilogue: dV (warpgroup 0) and scale * dK (warpgroup 1) -> 16-bit rows
+    // ---- epilogue (warpgroup 0): scale * dK -> 16-bit rows
     if (!ok) {
       wg_fail[wg] = 1;
       fail();
     }
-    if (!mbar_wait(acc_done, 0, abort_flag, lim)) {
-      wg_fail[wg] = 1;
+    if (wg == 0) {
+      if (!mbar_wait(acc_done, 0, abort_flag, lim)) {
+        wg_fail[0] = 1;
+        fail();
+      }
+      named_bar_sync_n(2, 128);
+      if (wg_fail[0] == 0) {
+        tc_fence_after();
+        uint16_t* out = p.dk + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::T_DK + 32u * c, v);
+          tmem_wait_ld();
+          if (key < N) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 o;
+              o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]) * p.scale, __uint_as_float(v[8 * u + 1]) * p.scale);
+              o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]) * p.scale, __uint_as_float(v[8 * u + 3]) * p.scale);
+              o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]) * p.scale, __uint_as_float(v[8 * u + 5]) * p.scale);
+              o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]) * p.scale, __uint_as_float(v[8 * u + 7]) * p.scale);
+              *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    setmaxnreg_dec<112>();
+    // ------------------------------------------- dQ^T -> fp32 accumulator
+    // Thread r holds row d = r of dQ^T (64 query columns).  Each 32-query half is staged
+    // as [d rows x 128 B] with the 128-byte swizzle and added into the accumulator
+    // ([B*Hq, d, Npad] fp32, queries contiguous) by one TMA bulk tensor reduction.
+    bool ok = true;
+    for (int it = 0; it < T; ++it) {
+      const int hq = hkv * G + it / nq;
+      const int q0 = 64 * (qb0 + it % nq);
+      if (!__all_sync(FULL, mbar_wait(dq_full, it & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tbase + lane_off + C::T_DQ, v);
+      tmem_ld32(tbase + lane_off + C::T_DQ + 32u, v + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      if (r == 0) bulk_wait_group_read0();  // the previous step's reductions have read the staging
+      named_bar_sync_n(1, 128);
+      if (r < D) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint8_t* rowp = smem + C::OFF_DQ + hh * C::DQ_HALF + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+                make_uint4(v[32 * hh + 4 * u], v[32 * hh + 4 * u + 1], v[32 * hh + 4 * u + 2], v[32 * hh + 4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync_n(1, 128);
+      if (r == 0) {
+        const int bh = b * p.Hq + hq;
+        tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQ, q0, 0, bh);
+        tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQ + C::DQ_HALF, q0 + 32, 0, bh);
+        bulk_commit_group();
+      }
+    }
+    if (r == 0) bulk_wait_group0();
+    // ---- epilogue: dV -> 16-bit rows
+    if (!ok) {
+      wg_fail[2] = 1;
       fail();
     }
-    named_bar_sync_n(3 + wg, 128);
-    if (wg_fail[wg] == 0) {
+    if (!mbar_wait(acc_done, 0, abort_flag, lim)) {
+      wg_fail[2] = 1;
+      fail();
+    }
+    named_bar_sync_n(3, 128);
+    if (wg_fail[2] == 0) {
       tc_fence_after();
       const int key = k0 + r;
-      uint16_t* out = (wg == 0 ? p.dv : p.dk) + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
-      const float mul = wg == 0 ? 1.0f : p.scale;
-      const uint32_t col = wg == 0 ? C::T_DV : C::T_DK;
+      uint16_t* out = p.dv + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tbase + lane_off + col + 32u * c, v);
+        tmem_ld32(tbase + lane_off + C::T_DV + 32u * c, v);
         tmem_wait_ld();
         if (key < N) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 o;
-            o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
-            o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
-            o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
-            o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+            o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+            o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+            o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+            o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
             *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
           }
         }
@@ -555,7 +611,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_main(const __grid_constant__ Bw
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
@@ -585,10 +641,8 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
-    const long long n8 = rows * D / 8;
-    const long long want = (n8 + 255) / 256;
-    const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
-    fa_bwd_dq_convert<BF16><<<grid, 256, 0, stream>>>(p.dq_acc, p.dq, n8, p.scale);
+    const long long grid = static_cast<long long>(p.B) * p.Hq * ((p.N + 63) / 64);
+    fa_bwd_dq_convert<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
     return cudaGetLastError();
   }
 }

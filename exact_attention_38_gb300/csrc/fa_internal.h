@@ -35,14 +35,14 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
   CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
-  CUtensorMap tm_dq;        // fp32 dQ accumulator [B, N, Hq, d], box {d, 1, 64, 1}, no swizzle
+  CUtensorMap tm_dq;        // fp32 dQ accumulator [B*Hq, d, Npad], box {32, d, 1}, 128-byte swizzle
   const uint16_t* o;        // [B, N, Hq, d] (preprocess)
   const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
   const float* lse;         // [B, Hq, N]
   uint16_t* dq;             // [B, N, Hq, d]
   uint16_t* dk;             // [B, N, Hkv, d]
   uint16_t* dv;             // [B, N, Hkv, d]
-  float* dq_acc;            // workspace: fp32 [B, N, Hq, d]
+  float* dq_acc;            // workspace: fp32 [B*Hq, d, Npad] (queries contiguous)
   float* dvec;              // workspace: -D = -rowsum(dO*O), [B*Hq, Npad] (0 past N)
   float* l2vec;             // workspace: -lse * log2(e), [B*Hq, Npad] (-inf past N)
   unsigned* err;
@@ -57,8 +57,8 @@ struct BwdWorkspace {
 };
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d);
 
-// 4-D map over the fp32 dQ accumulator [B, N, H, d], box = {d, 1, 64, 1}, no swizzle.
-bool encode_dq_acc_map(CUtensorMap* map, const float* base, int B, int N, int H, int d);
+// 3-D map over the fp32 dQ accumulator [B*Hq, d, Npad], box = {32, d, 1}, 128-byte swizzle.
+bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, int d);
 
 unsigned* device_error_word();  // address of this device's error word (device memory)
 

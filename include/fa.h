@@ -75,8 +75,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ accumulator
- * [B,N,Hq,d], then -D = -rowsum(dO * O) and -lse * log2(e), each [B*Hq, Npad] fp32 with
- * Npad = N rounded up to a multiple of 64; each part rounded up to 256 bytes.
+ * [B*Hq, d, Npad] (queries contiguous), then -D = -rowsum(dO * O) and -lse * log2(e),
+ * each [B*Hq, Npad] fp32, with Npad = N rounded up to a multiple of 64; each part
+ * rounded up to 256 bytes.
  * Returns 0 for invalid or unsupported sizes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);

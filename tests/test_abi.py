@@ -91,7 +91,7 @@ def test_workspace_size(lib):
     rows = B * Hq * N
     npad = (N + 63) // 64 * 64
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    want = up(rows * d * 4) + 2 * up(B * Hq * npad * 4)
+    want = up(B * Hq * d * npad * 4) + 2 * up(B * Hq * npad * 4)
     assert lib.fa_bwd_workspace_size(B, Hq, 2, N, d) == want
     assert lib.fa_bwd_workspace_size(B, Hq, 3, N, d) == 0
     assert lib.fa_bwd_workspace_size(B, Hq, 2, N, 80) == 0
