@@ -2,6 +2,7 @@
 // Every argument check happens before the first CUDA call, so a bad call returns
 // an error code without touching the device (and works on a host without a GPU).
 #include "fa_internal.h"
+#include "sm100_ptx.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -109,6 +110,19 @@ bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Waits on an mbarrier that no thread ever arrives on, through the same bounded wait the
+// attention kernels use; the wait gives up after `limit_ns` and records the timeout.
+__global__ void fa_selftest_wait_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(smem_u32(&bar), 0, nullptr, limit_ns);
+  if (!ok && threadIdx.x == 0) atomicOr(err, kDevErrTimeout);
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -192,6 +206,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.wait_limit_ns = kWaitLimitNs;
   const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_selftest_wait_timeout(int limit_us, fa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID;
+  unsigned* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  fa_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err,
+                                                                               static_cast<uint64_t>(limit_us) * 1000);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_check_device_error(fa_stream_t stream) {

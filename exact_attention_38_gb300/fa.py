@@ -45,6 +45,8 @@ def _load():
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_selftest_wait_timeout.argtypes = [i, vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -81,6 +83,11 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, 
 
 def fa_bwd_workspace_size(B, Hq, Hkv, N, d) -> int:
     return int(lib.fa_bwd_workspace_size(B, Hq, Hkv, N, d))
+
+
+def fa_selftest_wait_timeout(limit_us, stream) -> int:
+    """Mirror of the C ``fa_selftest_wait_timeout``."""
+    return lib.fa_selftest_wait_timeout(int(limit_us), stream)
 
 
 def fa_check_device_error(stream) -> int:

@@ -140,6 +140,16 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  */
 fa_status fa_check_device_error(fa_stream_t stream);
 
+/*
+ * Self-test of failure detection: launches one small kernel that waits, through the
+ * same bounded wait the attention kernels use, on a barrier nothing ever arrives on,
+ * with a limit of `limit_us` microseconds (1 .. 1000000).  The wait gives up, the kernel
+ * records the timeout in the device error word and exits normally, so the context stays
+ * usable.  Returns FA_OK once enqueued (FA_ERR_INVALID for a limit out of range); the
+ * next fa_check_device_error() on the stream reports FA_ERR_TIMEOUT.
+ */
+fa_status fa_selftest_wait_timeout(int limit_us, fa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 
