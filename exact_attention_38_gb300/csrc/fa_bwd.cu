@@ -18,13 +18,16 @@
 // fa_bwd_main: one CTA per (batch, key/value head, block of 128 keys).  K_j and V_j stay
 // in shared memory; the CTA walks every query head of its GQA group and every visible
 // block of 64 queries.  Per step the tensor cores compute S^T = K Q^T and dP^T = V dO^T
-// into tensor memory (S^T double-buffered); two softmax warpgroups (thread = key row =
-// TMEM lane, each taking 32 of the 64 query columns) turn them into P^T (written back
-// to TMEM as 16-bit pairs) and dS^T (written to swizzled shared memory); the tensor
-// cores then accumulate dV += P^T dO and dK += dS^T Q in TMEM for the whole walk and
-// compute dQ^T = K^T dS^T, which a fourth warpgroup stages in shared memory and adds
-// into the fp32 dQ accumulator with TMA bulk tensor reductions while the next step's
-// S^T / dP^T run.
+// into tensor memory (S^T double-buffered, K itself held in TMEM as the A operand);
+// two softmax warpgroups (thread = key row = TMEM lane, each taking 32 of the 64 query
+// columns) turn them into P^T and dS^T, both written back as 16-bit pairs into the S^T
+// columns they read (dS^T also to swizzled shared memory); the tensor cores then accumulate
+// dV += P^T dO and dK += dS^T Q in TMEM for the whole walk (A operands from TMEM) and
+// compute dQ^T = K^T dS^T into the same S^T buffer, which a fourth warpgroup stages in
+// shared memory and adds into the fp32 dQ accumulator with TMA bulk tensor reductions
+// while the next step's S^T / dP^T run.  Taking operands from TMEM matters because the
+// tensor cores read shared-memory operands at 128 B/clk per SM, which otherwise bounds
+// this kernel.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -49,8 +52,8 @@ struct BwdCfg {
   static constexpr int THREADS = 512;
   // barrier indices
   static constexpr int B_KV = 0, B_SDP = 1, B_DPFREE = 2, B_DSREADY = 3 /*[2]*/, B_DSFREE = 5 /*[2]*/,
-                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_STFULL = 11 /*[STG]*/;
-  static constexpr int NBARS = 11 + 2 * STG;
+                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_KTM = 11, B_STFULL = 12 /*[STG]*/;
+  static constexpr int NBARS = 12 + 2 * STG;
   // shared-memory layout (offsets from the 1024-aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
@@ -62,8 +65,9 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 8 * NBARS + 64;
   static_assert(SMEM <= 232448, "shared memory budget");
-  // tensor-memory columns
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
+  // tensor-memory columns: S^T[2] (each later holding P^T | dS^T, then dQ^T), dP^T,
+  // K (16-bit pairs, the A operand of S^T), dV, dK
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_K = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   auto bar = [&](int i) { return bar0 + 8u * i; };
   const uint32_t kv_full = bar(C::B_KV), sdp_full = bar(C::B_SDP), dp_free = bar(C::B_DPFREE);
   const uint32_t dq_full = bar(C::B_DQFULL), dq_free = bar(C::B_DQFREE), acc_done = bar(C::B_ACC);
-  const uint32_t final_bar = bar(C::B_FINAL);
+  const uint32_t final_bar = bar(C::B_FINAL), k_tmem = bar(C::B_KTM);
   auto ds_ready = [&](int b) { return bar(C::B_DSREADY + b); };
   auto ds_free = [&](int b) { return bar(C::B_DSFREE + b); };
   auto st_full = [&](int s) { return bar(C::B_STFULL + s); };
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(final_bar, 1);
+    mbar_init(k_tmem, 128);
     for (int s = 0; s < C::STG; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 1);
@@ -326,17 +331,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       constexpr uint32_t id_grad = idesc_f16(128, D, bf, 0, 1);  // dV, dK: M=keys, N=d, B MN-major
       constexpr uint32_t id_dq = idesc_f16(128, 64, bf, 1, 1);   // dQ^T: M=d (padded to 128), N=queries
       // descriptor templates; per step only the start-address field (16-byte units) moves
-      const uint64_t dK_km = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
       const uint64_t dV_km = smem_desc_sw128(sbase + C::OFF_V, 16, 1024);
       const uint64_t dQ_km = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t dDO_km = smem_desc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t dQ_mn = smem_desc_sw128(sbase + C::OFF_Q, C::Q_CHUNK, 1024);
       const uint64_t dDO_mn = smem_desc_sw128(sbase + C::OFF_DO, C::Q_CHUNK, 1024);
-      const uint64_t dDS_km = smem_desc_sw128(sbase + C::OFF_DS, 16, 1024);
       const uint64_t dDS_mn = smem_desc_sw128(sbase + C::OFF_DS, 1024, 1024);
       const uint64_t dK_mn = smem_desc_sw128(sbase + C::OFF_K, C::KV_CHUNK, 1024);
       auto u16 = [](int bytes) { return static_cast<uint64_t>(bytes >> 4); };
-      bool ok = __all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim));
+      bool ok = __all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim) && mbar_wait(k_tmem, 0, abort_flag, lim));
       for (int it = 0; it <= T && ok; ++it) {
         if (it < T) {
           const int s = it % C::STG, bb = it & 1;
@@ -344,13 +347,18 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             ok = false;
             break;
           }
+          // S^T(it) overwrites the buffer that held dQ^T(it-2): it must have been read out
+          if (it >= 2 && !__all_sync(FULL, mbar_wait(dq_free, (it - 2) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint64_t qs = u16(s * C::Q_TILE);
-          // S^T = K Q^T  (both K-major)
+          // S^T = K Q^T  (K from TMEM as 16-bit pairs; Q K-major)
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tbase + C::T_S + 64u * bb, dK_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
+              mma_ts(tbase + C::T_S + 64u * bb, tbase + C::T_K + 8u * kk,
                      dQ_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
           }
           if (it > 0 && !__all_sync(FULL, mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim))) {
@@ -376,30 +384,30 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
           tc_fence_after();
           const uint64_t qs = u16(s * C::Q_TILE), dss = u16(bb * C::DS_TILE);
           if (leader) {
+            // k-step kk covers queries [16 kk, 16 kk + 16): in the S^T buffer, queries
+            // [32 h, 32 h + 32) hold P^T in columns [32 h, 32 h + 16) and dS^T in
+            // [32 h + 16, 32 h + 32), as 16-bit pairs
             // dV += P^T dO   (P^T from TMEM; dO MN-major: queries x d)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tbase + C::T_DV, tbase + C::T_S + 64u * bb + 8u * kk, dDO_mn + qs + u16(kk * 2048), id_grad,
-                     (i > 0 || kk > 0));
-            // dK += dS^T Q   (dS^T K-major in shared memory; Q MN-major)
+              mma_ts(tbase + C::T_DV, tbase + C::T_S + 64u * bb + 32u * (kk / 2) + 8u * (kk % 2),
+                     dDO_mn + qs + u16(kk * 2048), id_grad, (i > 0 || kk > 0));
+            // dK += dS^T Q   (dS^T from TMEM; Q MN-major)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tbase + C::T_DK, dDS_km + dss + u16(kk * 32), dQ_mn + qs + u16(kk * 2048), id_grad,
-                     (i > 0 || kk > 0));
+              mma_ts(tbase + C::T_DK, tbase + C::T_S + 64u * bb + 32u * (kk / 2) + 16u + 8u * (kk % 2),
+                     dQ_mn + qs + u16(kk * 2048), id_grad, (i > 0 || kk > 0));
             // the stage's Q / dO are no longer read once these complete
             mma_commit(st_empty(s));
           }
-          if (i > 0 && !__all_sync(FULL, mbar_wait(dq_free, (i - 1) & 1, abort_flag, lim))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           if (leader) {
-            // dQ^T = K^T dS^T  (K^T: MN-major view of the K tile, d padded to 128 rows;
-            // dS^T: MN-major, queries contiguous)
+            // dQ^T = K^T dS^T into the step's S^T buffer, after dV and dK above have read
+            // P^T and dS^T from it (tcgen05.mma executes in issue order).  K^T: MN-major
+            // view of the K tile, d padded to 128 rows; dS^T: MN-major, queries contiguous.
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tbase + C::T_DQ, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq, kk > 0);
+              mma_ss(tbase + C::T_S + 64u * bb, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq,
+                     kk > 0);
             mma_commit(dq_full);
             mma_commit(ds_free(bb));
           }
@@ -422,7 +430,31 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     const uint64_t cl2x2 = f2pack(cl2, cl2);
     const int key = k0 + r;
     const int cbase = 32 * wg;
-    for (int it = 0; it < T; ++it) {
+    if (wg == 0) {
+      // K row r -> TMEM lane r as 16-bit pairs (the A operand of S^T = K Q^T)
+      if (!__all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim))) {
+        ok = false;
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          uint32_t kr[32];
+          const uint8_t* rowp = smem + C::OFF_K + ch * C::KV_CHUNK + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 q4 = *reinterpret_cast<const uint4*>(rowp + ((u ^ (r & 7)) * 16));
+            kr[4 * u] = q4.x;
+            kr[4 * u + 1] = q4.y;
+            kr[4 * u + 2] = q4.z;
+            kr[4 * u + 3] = q4.w;
+          }
+          tmem_st32(tbase + lane_off + C::T_K + 32u * ch, kr);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(k_tmem);
+      }
+    }
+    for (int it = 0; it < T && ok; ++it) {
       const int s = it % C::STG, bb = it & 1;
       const int q0 = 64 * (qb0 + it % nq);
       if (!__all_sync(FULL, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim) &&
@@ -451,10 +483,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       // dS^T row r -> 128-byte swizzled row of the [128 keys x 64 queries] tile; this
       // warpgroup writes 16-byte units [4 wg, 4 wg + 4)
       uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
-      uint32_t pk[16];
+      uint32_t pk[16], dsk[16];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        uint32_t dk2[4];
+        uint32_t* dk2 = dsk + 4 * g;
 #pragma unroll
         for (int h4 = 0; h4 < 2; ++h4) {
           const int c4 = 2 * g + h4;
@@ -492,8 +524,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         }
         *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
       }
-      // P^T: 32 queries -> 16 packed columns at [16 wg, 16 wg + 16) of S^T's buffer
-      tmem_st16(tbase + lane_off + C::T_S + 64u * bb + 16u * wg, pk);
+      // P^T (16 packed columns) then dS^T (16) go back into the 32 columns of S^T this
+      // warpgroup read, so neither warpgroup writes columns the other still reads
+      tmem_st16(tbase + lane_off + C::T_S + 64u * bb + cbase, pk);
+      tmem_st16(tbase + lane_off + C::T_S + 64u * bb + cbase + 16u, dsk);
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
@@ -548,8 +582,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       }
       tc_fence_after();
       uint32_t v[64];
-      tmem_ld32(tbase + lane_off + C::T_DQ, v);
-      tmem_ld32(tbase + lane_off + C::T_DQ + 32u, v + 32);
+      const uint32_t dq_tm = tbase + lane_off + C::T_S + 64u * (it & 1);
+      tmem_ld32(dq_tm, v);
+      tmem_ld32(dq_tm + 32u, v + 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(dq_free);
