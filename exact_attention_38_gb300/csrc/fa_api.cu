@@ -226,7 +226,7 @@ fa_status fa_check_device_error(fa_stream_t stream) {
   if (h != 0) {
     const unsigned z = 0;
     if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    return (h & kDevErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
   }
   return FA_OK;
 }

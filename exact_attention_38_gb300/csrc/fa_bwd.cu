@@ -18,7 +18,7 @@
 // fa_bwd_main: one CTA per (batch, key/value head, block of 128 keys).  K_j and V_j stay
 // in shared memory; the CTA walks every query head of its GQA group and every visible
 // block of 64 queries.  Per step the tensor cores compute S^T = K Q^T and dP^T = V dO^T
-// into tensor memory (S^T double-buffered, K itself held in TMEM as the A operand);
+// into tensor memory (S^T double-buffered, V itself held in TMEM as the A operand);
 // two softmax warpgroups (thread = key row = TMEM lane, each taking 32 of the 64 query
 // columns) turn them into P^T and dS^T, both written back as 16-bit pairs into the S^T
 // columns they read (dS^T also to swizzled shared memory); the tensor cores then accumulate
@@ -48,26 +48,30 @@ struct BwdCfg {
   static constexpr int Q_TILE = 64 * D * 2;       // Q or dO tile
   static constexpr int DS_TILE = 128 * 64 * 2;    // dS^T tile, 128 keys x 64 queries, 16-bit
   static constexpr int DQ_HALF = D * 128;         // dQ^T staging: D rows x 32 fp32 queries (128 B)
-  static constexpr int STG = (D == 128) ? 3 : 5;  // Q/dO/lse/D stages
+  static constexpr int STG = (D == 128) ? 4 : 6;  // Q/dO/lse/D stages
   static constexpr int THREADS = 512;
   // barrier indices
   static constexpr int B_KV = 0, B_SDP = 1, B_DPFREE = 2, B_DSREADY = 3 /*[2]*/, B_DSFREE = 5 /*[2]*/,
-                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_KTM = 11, B_STFULL = 12 /*[STG]*/;
+                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_VTM = 11, B_STFULL = 12 /*[STG]*/;
   static constexpr int NBARS = 12 + 2 * STG;
-  // shared-memory layout (offsets from the 1024-aligned base)
+  // shared-memory layout (offsets from the 1024-aligned base).  V is loaded into the
+  // dS^T buffers, copied into TMEM, and never read from shared memory again.
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KV_TILE;
-  static constexpr int OFF_Q = 2 * KV_TILE;                    // [STG] Q tiles
+  static constexpr int OFF_Q = KV_TILE;                        // [STG] Q tiles
   static constexpr int OFF_DO = OFF_Q + STG * Q_TILE;          // [STG] dO tiles
-  static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles
+  static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles (V first)
+  static constexpr int OFF_V = OFF_DS;
+  static_assert(2 * DS_TILE >= KV_TILE, "V fits in the dS^T buffers");
   static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;          // [2] dQ^T staging halves
   static constexpr int OFF_LD = OFF_DQ + 2 * DQ_HALF;          // [STG][2][64] floats: -lse*log2e, -D
   static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
-  static constexpr int SMEM = 1024 + OFF_BAR + 8 * NBARS + 64;
+  // no alignment slack: the dynamic shared-memory base is 1024-byte aligned (checked at
+  // run time by the kernel)
+  static constexpr int SMEM = OFF_BAR + 8 * NBARS + 64;
   static_assert(SMEM <= 232448, "shared memory budget");
   // tensor-memory columns: S^T[2] (each later holding P^T | dS^T, then dQ^T), dP^T,
-  // K (16-bit pairs, the A operand of S^T), dV, dK
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_K = 192, T_DV = 256, T_DK = 256 + D;
+  // V (16-bit pairs, the A operand of dP^T), dV, dK
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_V = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -197,8 +201,14 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_bwd[];
+  // the 128-byte-swizzled tiles need 1024-byte alignment; with a misaligned base the
+  // kernel records an error and does nothing (uniform early exit, before any barrier)
+  if ((smem_u32(smem_bwd) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, kDevErrLayout);
+    return;
+  }
+  uint8_t* smem = smem_bwd;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   auto bar = [&](int i) { return bar0 + 8u * i; };
   const uint32_t kv_full = bar(C::B_KV), sdp_full = bar(C::B_SDP), dp_free = bar(C::B_DPFREE);
   const uint32_t dq_full = bar(C::B_DQFULL), dq_free = bar(C::B_DQFREE), acc_done = bar(C::B_ACC);
-  const uint32_t final_bar = bar(C::B_FINAL), k_tmem = bar(C::B_KTM);
+  const uint32_t final_bar = bar(C::B_FINAL), v_tmem = bar(C::B_VTM);
   auto ds_ready = [&](int b) { return bar(C::B_DSREADY + b); };
   auto ds_free = [&](int b) { return bar(C::B_DSFREE + b); };
   auto st_full = [&](int s) { return bar(C::B_STFULL + s); };
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(final_bar, 1);
-    mbar_init(k_tmem, 128);
+    mbar_init(v_tmem, 128);
     for (int s = 0; s < C::STG; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 1);
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       constexpr uint32_t id_grad = idesc_f16(128, D, bf, 0, 1);  // dV, dK: M=keys, N=d, B MN-major
       constexpr uint32_t id_dq = idesc_f16(128, 64, bf, 1, 1);   // dQ^T: M=d (padded to 128), N=queries
       // descriptor templates; per step only the start-address field (16-byte units) moves
-      const uint64_t dV_km = smem_desc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t dK_km = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
       const uint64_t dQ_km = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t dDO_km = smem_desc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t dQ_mn = smem_desc_sw128(sbase + C::OFF_Q, C::Q_CHUNK, 1024);
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       const uint64_t dDS_mn = smem_desc_sw128(sbase + C::OFF_DS, 1024, 1024);
       const uint64_t dK_mn = smem_desc_sw128(sbase + C::OFF_K, C::KV_CHUNK, 1024);
       auto u16 = [](int bytes) { return static_cast<uint64_t>(bytes >> 4); };
-      bool ok = __all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim) && mbar_wait(k_tmem, 0, abort_flag, lim));
+      bool ok = __all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim) && mbar_wait(v_tmem, 0, abort_flag, lim));
       for (int it = 0; it <= T && ok; ++it) {
         if (it < T) {
           const int s = it % C::STG, bb = it & 1;
@@ -354,11 +364,11 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
           }
           tc_fence_after();
           const uint64_t qs = u16(s * C::Q_TILE);
-          // S^T = K Q^T  (K from TMEM as 16-bit pairs; Q K-major)
+          // S^T = K Q^T  (both K-major in shared memory)
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ts(tbase + C::T_S + 64u * bb, tbase + C::T_K + 8u * kk,
+              mma_ss(tbase + C::T_S + 64u * bb, dK_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
                      dQ_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
           }
           if (it > 0 && !__all_sync(FULL, mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim))) {
@@ -366,11 +376,11 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             break;
           }
           tc_fence_after();
-          // dP^T = V dO^T
+          // dP^T = V dO^T  (V from TMEM as 16-bit pairs; dO K-major)
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tbase + C::T_DP, dV_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
+              mma_ts(tbase + C::T_DP, tbase + C::T_V + 8u * kk,
                      dDO_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
             mma_commit(sdp_full);
           }
@@ -431,14 +441,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     const int key = k0 + r;
     const int cbase = 32 * wg;
     if (wg == 0) {
-      // K row r -> TMEM lane r as 16-bit pairs (the A operand of S^T = K Q^T)
+      // V row r -> TMEM lane r as 16-bit pairs (the A operand of dP^T = V dO^T); V's
+      // shared-memory copy sits in the dS^T buffers, which are written only after this
       if (!__all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim))) {
         ok = false;
       } else {
 #pragma unroll
         for (int ch = 0; ch < C::CHUNKS; ++ch) {
           uint32_t kr[32];
-          const uint8_t* rowp = smem + C::OFF_K + ch * C::KV_CHUNK + r * 128;
+          const uint8_t* rowp = smem + C::OFF_V + ch * C::KV_CHUNK + r * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const uint4 q4 = *reinterpret_cast<const uint4*>(rowp + ((u ^ (r & 7)) * 16));
@@ -447,12 +458,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             kr[4 * u + 2] = q4.z;
             kr[4 * u + 3] = q4.w;
           }
-          tmem_st32(tbase + lane_off + C::T_K + 32u * ch, kr);
+          tmem_st32(tbase + lane_off + C::T_V + 32u * ch, kr);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(k_tmem);
+        mbar_arrive(v_tmem);
       }
+    } else if (!__all_sync(FULL, mbar_wait(v_tmem, 0, abort_flag, lim))) {
+      ok = false;  // warpgroup 1 writes dS^T over V's shared-memory copy: wait for the copy
     }
     for (int it = 0; it < T && ok; ++it) {
       const int s = it % C::STG, bb = it & 1;

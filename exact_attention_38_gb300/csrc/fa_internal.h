@@ -10,8 +10,10 @@
 
 namespace fa {
 
-// Device error word bits (set by kernels whose bounded waits ran out).
+// Device error word bits: a bounded wait ran out / a launch found its shared-memory
+// base misaligned (did no work).
 constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrLayout = 2u;
 
 // Bounded waits give up after this long (ns); a pipeline stage normally waits
 // microseconds, so only a broken pipeline gets near it.

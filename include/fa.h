@@ -136,7 +136,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 /*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting and wound down without
- * finishing its work; its outputs are undefined) or FA_ERR_CUDA.
+ * finishing its work; its outputs are undefined) or FA_ERR_CUDA (a CUDA call failed,
+ * or a kernel found its launch unusable, e.g. a misaligned shared-memory base, and did
+ * no work).
  */
 fa_status fa_check_device_error(fa_stream_t stream);
 
