@@ -51,9 +51,13 @@ struct BwdCfg {
   static constexpr int STG = (D == 128) ? 4 : 6;  // Q/dO/lse/D stages
   static constexpr int THREADS = 512;
   // barrier indices
+  // dq_full has one barrier per dQ^T buffer: with a single one the MMA could complete the
+  // phases of two consecutive steps before the dQ warpgroup polls the first of them, and
+  // the parity it then sees would look unchanged
   static constexpr int B_KV = 0, B_SDP = 1, B_DPFREE = 2, B_DSREADY = 3 /*[2]*/, B_DSFREE = 5 /*[2]*/,
-                       B_DQFULL = 7, B_DQFREE = 8, B_ACC = 9, B_FINAL = 10, B_VTM = 11, B_STFULL = 12 /*[STG]*/;
-  static constexpr int NBARS = 12 + 2 * STG;
+                       B_DQFULL = 7 /*[2]*/, B_DQFREE = 9, B_ACC = 10, B_FINAL = 11, B_VTM = 12,
+                       B_STFULL = 13 /*[STG]*/;
+  static constexpr int NBARS = 13 + 2 * STG;
   // shared-memory layout (offsets from the 1024-aligned base).  V is loaded into the
   // dS^T buffers, copied into TMEM, and never read from shared memory again.
   static constexpr int OFF_K = 0;
@@ -213,14 +217,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [4]
+  volatile int* dq_fail = reinterpret_cast<volatile int*>(tmem_slot + 6);  // dQ warpgroup gave up
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * i; };
   const uint32_t kv_full = bar(C::B_KV), sdp_full = bar(C::B_SDP), dp_free = bar(C::B_DPFREE);
-  const uint32_t dq_full = bar(C::B_DQFULL), dq_free = bar(C::B_DQFREE), acc_done = bar(C::B_ACC);
+  const uint32_t dq_free = bar(C::B_DQFREE), acc_done = bar(C::B_ACC);
   const uint32_t final_bar = bar(C::B_FINAL), v_tmem = bar(C::B_VTM);
   auto ds_ready = [&](int b) { return bar(C::B_DSREADY + b); };
   auto ds_free = [&](int b) { return bar(C::B_DSFREE + b); };
+  auto dq_full = [&](int b) { return bar(C::B_DQFULL + b); };
   auto st_full = [&](int s) { return bar(C::B_STFULL + s); };
   auto st_empty = [&](int s) { return bar(C::B_STFULL + C::STG + s); };
   constexpr unsigned FULL = 0xffffffffu;
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     wg_fail[0] = wg_fail[1] = wg_fail[2] = wg_fail[3] = 0;
+    *dq_fail = 0;
     mbar_init(kv_full, 1);
     mbar_init(sdp_full, 1);
     mbar_init(dp_free, 256);
@@ -254,7 +261,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     mbar_init(ds_ready(1), 256);
     mbar_init(ds_free(0), 1);
     mbar_init(ds_free(1), 1);
-    mbar_init(dq_full, 1);
+    mbar_init(dq_full(0), 1);
+    mbar_init(dq_full(1), 1);
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(final_bar, 1);
@@ -418,7 +426,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tbase + C::T_S + 64u * bb, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq,
                      kk > 0);
-            mma_commit(dq_full);
+            mma_commit(dq_full(bb));
             mma_commit(ds_free(bb));
           }
         }
@@ -429,6 +437,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         mma_commit(final_bar);
       }
       mbar_wait(final_bar, 0, nullptr, lim);
+      // The last commits to st_empty and ds_free have no consumer; let their arrivals land
+      // before this CTA's shared memory (and the barriers in it) passes to the next CTA.
+      if (ok) {
+        for (int i = (T > C::STG ? T - C::STG : 0); i < T; ++i)
+          mbar_wait(st_empty(i % C::STG), (i / C::STG) & 1, nullptr, lim);
+        for (int i = (T > 2 ? T - 2 : 0); i < T; ++i) mbar_wait(ds_free(i & 1), (i >> 1) & 1, nullptr, lim);
+      }
       __syncwarp();
     }
   } else if (wg < 2) {
@@ -589,20 +604,29 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     for (int it = 0; it < T; ++it) {
       const int hq = hkv * G + it / nq;
       const int q0 = 64 * (qb0 + it % nq);
-      if (!__all_sync(FULL, mbar_wait(dq_full, it & 1, abort_flag, lim))) {
+      // The named barriers below span the four warps of this warpgroup, but a wait's
+      // outcome is only warp-uniform: a warp that gives up records it in dq_fail and
+      // still arrives at the barrier, after which all four warps read the same flag and
+      // leave together (no warp is left waiting at a barrier the others skipped).
+      const bool got = __all_sync(FULL, mbar_wait(dq_full(it & 1), (it >> 1) & 1, abort_flag, lim));
+      uint32_t v[64];
+      if (got) {
+        tc_fence_after();
+        const uint32_t dq_tm = tbase + lane_off + C::T_S + 64u * (it & 1);
+        tmem_ld32(dq_tm, v);
+        tmem_ld32(dq_tm + 32u, v + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_free);
+      } else if (lane == 0) {
+        *dq_fail = 1;
+      }
+      if (r == 0) bulk_wait_group_read0();  // the previous step's reductions have read the staging
+      named_bar_sync_n(1, 128);
+      if (*dq_fail) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      uint32_t v[64];
-      const uint32_t dq_tm = tbase + lane_off + C::T_S + 64u * (it & 1);
-      tmem_ld32(dq_tm, v);
-      tmem_ld32(dq_tm + 32u, v + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(dq_free);
-      if (r == 0) bulk_wait_group_read0();  // the previous step's reductions have read the staging
-      named_bar_sync_n(1, 128);
       if (r < D) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {

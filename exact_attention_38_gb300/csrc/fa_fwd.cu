@@ -264,6 +264,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     // every MMA the leader issued must be finished before TMEM is released
     if (leader) mma_commit(final_bar);
     mbar_wait(final_bar, 0, no_abort, lim);
+    // The last commits to kv_empty have no consumer; let their arrivals land before this
+    // CTA's shared memory (and the barriers in it) passes to the next CTA.
+    if (ok) {
+      for (int c = (2 * nmax > C::STAGES ? 2 * nmax - C::STAGES : 0); c < 2 * nmax; ++c)
+        mbar_wait(kv_empty(c % C::STAGES), (c / C::STAGES) & 1, no_abort, lim);
+    }
     __syncwarp();
    }
   } else {

@@ -19,7 +19,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Barrier over `nthreads` threads (a multiple of 32) with id 1..15 (0 is __syncthreads).
+// bar.sync counts whole warps: if part of a warp reaches it while other lanes are still
+// in a divergent branch, the warp is counted as arrived and the late lanes arrive at
+// the next generation of the barrier, desynchronising the warpgroup.  The compiler does
+// not treat this inline instruction as a barrier, so the warp is reconverged explicitly.
 __device__ __forceinline__ void named_bar_sync_n(int id, int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
