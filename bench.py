@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--Hkv", type=int, default=None, help="key/value heads (default: --H, i.e. MHA)")
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -51,7 +52,8 @@ def parse():
 
 def workload(a):
     B = a.B if a.B is not None else max(1, 16384 // a.N)
-    return dict(B=B, Hq=a.H, Hkv=a.H, N=a.N, d=a.d, causal=bool(a.causal), dtype="bf16")
+    Hkv = a.Hkv if a.Hkv is not None else a.H
+    return dict(B=B, Hq=a.H, Hkv=Hkv, N=a.N, d=a.d, causal=bool(a.causal), dtype="bf16")
 
 
 def flops(w, which):
@@ -64,7 +66,7 @@ def flops(w, which):
 def workload_name(w, which):
     passes = {"step": "fwd+bwd", "fwd": "fwd", "bwd": "bwd"}[which]
     return (f"exact attention {passes}, B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} N={w['N']} d={w['d']} "
-            f"{w['dtype']} {'causal' if w['causal'] else 'non-causal'} (16k tokens/batch)")
+            f"{w['dtype']} {'causal' if w['causal'] else 'non-causal'} ({w['B'] * w['N'] // 1024}k tokens/batch)")
 
 
 def kernel_source_digest(kernel):
