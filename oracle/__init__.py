@@ -15,3 +15,10 @@ from .attention import (  # noqa: F401
     attn_probs,
     brute_force_fwd,
 )
+from .varlen import (  # noqa: F401
+    attn_bwd_qk,
+    attn_fwd_qk,
+    attn_varlen_bwd_ref,
+    attn_varlen_fwd_ref,
+    brute_force_fwd_qk,
+)
