@@ -55,6 +55,27 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int dty
   return FA_OK;
 }
 
+// Shape checks of the variable-length entry points (the per-sequence offsets live in
+// device memory and are checked by the kernels).
+fa_status check_varlen(int B, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k, int d, float scale,
+                       int dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0)
+    return FA_ERR_INVALID;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (max_q > (1 << 20) || max_k > (1 << 20) || B > (1 << 20)) return FA_ERR_UNSUPPORTED;
+  const long long tq = static_cast<long long>(total_q) * Hq * d * 2, tk = static_cast<long long>(total_k) * Hkv * d * 2;
+  if (tq >= (1LL << 40) || tk >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  const long long tiles = static_cast<long long>(B) * Hq * ((max_q + 255) / 256);
+  const long long kblocks = static_cast<long long>(B) * Hkv * ((max_k + 127) / 128);
+  if (tiles >= (1LL << 31) || kblocks >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 }  // namespace
 
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d) {
@@ -93,6 +114,24 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r =
       enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d, int box_rows, fa_dtype dtype) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  // an empty packed tensor is never read (every sequence has length 0); the map still
+  // needs one row to be encodable
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(total > 0 ? total : 1)};
+  const cuuint64_t es = 2;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(H) * d * es};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -159,7 +198,42 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
-  const cudaError_t e = launch_fwd(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_fwd(p, d, dtype, causal != 0, false, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, const int* seqused_q, const int* seqused_k, int B, int Hq, int Hkv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale,
+                        fa_dtype dtype, fa_stream_t stream) {
+  if (!aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k)) return FA_ERR_INVALID;
+  if ((seqused_q && !aligned4(seqused_q)) || (seqused_k && !aligned4(seqused_k))) return FA_ERR_INVALID;
+  const fa_status st =
+      check_varlen(B, Hq, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query row to write
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+  if (total_k > 0 && (!aligned16(k) || !aligned16(v))) return FA_ERR_INVALID;
+  // with no key row at all the key/value maps are never read; they are encoded over q
+  const void* kb = total_k > 0 ? k : q;
+  const void* vb = total_k > 0 ? v : q;
+  FwdParams p{};
+  if (!encode_thd_map(&p.tm_q, q, total_q, Hq, d, 128, dtype) || !encode_thd_map(&p.tm_k, kb, total_k, Hkv, d, 128, dtype) ||
+      !encode_thd_map(&p.tm_v, vb, total_k, Hkv, d, 128, dtype) || !encode_thd_map(&p.tm_o, o, total_q, Hq, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  p.lse = lse;
+  p.o = static_cast<uint16_t*>(o);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.vl = Seqlens{cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, total_q, total_k, max_seqlen_q, max_seqlen_k};
+  const cudaError_t e = launch_fwd(p, d, dtype, causal != 0, true, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -204,7 +278,68 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
-  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, false, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+static int varlen_npad(int max_q) { return max_q > 0 ? (max_q + 63) / 64 * 64 : 64; }
+
+size_t fa_bwd_varlen_workspace_size(int B, int Hq, int max_seqlen_q, int d) {
+  if (check_varlen(B, Hq, 1, 0, 0, max_seqlen_q, 0, d, 1.0f, FA_BF16) != FA_OK) return 0;
+  return bwd_workspace_layout(B, Hq, varlen_npad(max_seqlen_q), d).total;
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, const int* seqused_q, const int* seqused_k, int B, int Hq, int Hkv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale,
+                        fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k)) return FA_ERR_INVALID;
+  if ((seqused_q && !aligned4(seqused_q)) || (seqused_k && !aligned4(seqused_k))) return FA_ERR_INVALID;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  const fa_status st =
+      check_varlen(B, Hq, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, static_cast<int>(dtype));
+  if (st != FA_OK) return st;
+  const int npad = varlen_npad(max_seqlen_q);
+  const BwdWorkspace ws = bwd_workspace_layout(B, Hq, npad, d);
+  if (workspace_bytes < ws.total) return FA_ERR_INVALID;
+  if (total_q == 0 && total_k == 0) return FA_OK;  // nothing to write
+  if (total_q > 0 && (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq)))
+    return FA_ERR_INVALID;
+  if (total_k > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))) return FA_ERR_INVALID;
+  // an empty side is never read (every sequence has length 0 there); its maps are
+  // encoded over the other side's tensors
+  const void* qb = total_q > 0 ? q : k;
+  const void* dob = total_q > 0 ? dout : k;
+  const void* kb = total_k > 0 ? k : q;
+  const void* vb = total_k > 0 ? v : q;
+  BwdParams p{};
+  if (!encode_thd_map(&p.tm_q, qb, total_q, Hq, d, 64, dtype) || !encode_thd_map(&p.tm_do, dob, total_q, Hq, d, 64, dtype) ||
+      !encode_thd_map(&p.tm_k, kb, total_k, Hkv, d, 128, dtype) || !encode_thd_map(&p.tm_v, vb, total_k, Hkv, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
+  p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
+  p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
+  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, npad, d)) return FA_ERR_CUDA;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = 0;
+  p.Npad = npad;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.vl = Seqlens{cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, total_q, total_k, max_seqlen_q, max_seqlen_k};
+  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, true, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -226,7 +361,9 @@ fa_status fa_check_device_error(fa_stream_t stream) {
   if (h != 0) {
     const unsigned z = 0;
     if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return (h & kDevErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+    if (h & kDevErrTimeout) return FA_ERR_TIMEOUT;
+    if (h & kDevErrSeqlens) return FA_ERR_INVALID;
+    return FA_ERR_CUDA;
   }
   return FA_OK;
 }

@@ -172,16 +172,73 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
   for (long long i = tid; i < nacc4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Variable-length form: rows (b*Hq + h, n) of the padded layout, n < Npad; query n of
+// sequence b is packed row start_q + n.  A row whose lse is -inf (it sees no key) gets
+// -inf as well, so its P is 0.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess_varlen(const __grid_constant__ BwdParams p) {
+  constexpr int LPR = D / 8;
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Npad;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, part = lane % LPR;
+  const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  for (long long base = wid * (32 / LPR); base < rows; base += warps_total * (32 / LPR)) {
+    const long long r = base + sub;
+    const long long bh = r / p.Npad;
+    const int n = static_cast<int>(r % p.Npad);
+    const int b = static_cast<int>(bh / p.Hq), h = static_cast<int>(bh % p.Hq);
+    int sq = 0, lq = 0, sk = 0, lk = 0;
+    const bool live = r < rows && seq_span(p.vl, b, sq, lq, sk, lk) && n < lq;
+    float acc = 0.f;
+    if (live) {
+      const long long off = (static_cast<long long>(sq + n) * p.Hq + h) * D + part * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
+      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        acc += bw_unpack_lo<BF16>(av[i]) * bw_unpack_lo<BF16>(gv[i]) +
+               bw_unpack_hi<BF16>(av[i]) * bw_unpack_hi<BF16>(gv[i]);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (r < rows && part == 0) {
+      float l2 = -INFINITY;
+      if (live) {
+        const float lse = p.lse[static_cast<long long>(h) * p.vl.total_q + sq + n];
+        l2 = lse == -INFINITY ? -INFINITY : -lse * kLog2e;
+      }
+      p.dvec[bh * p.Npad + n] = live ? -acc : 0.f;
+      p.l2vec[bh * p.Npad + n] = l2;
+    }
+  }
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long nacc4 = static_cast<long long>(p.B) * p.Hq * D * p.Npad / 4;
+  float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+  for (long long i = tid; i < nacc4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // ------------------------------------------------------------------ dQ convert
 // dQ[b, n, h, :] = scale * acc[b*Hq + h, :, n]: a tiled transpose through shared memory
 // (coalesced fp32 reads along n, coalesced 16-bit writes along d).
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__ BwdParams p) {
   __shared__ float tile[D][65];
-  const int nblk = (p.N + 63) / 64;
+  const int nblk = VARLEN ? p.Npad / 64 : (p.N + 63) / 64;
   const int bh = static_cast<int>(blockIdx.x / nblk);
   const int n0 = 64 * static_cast<int>(blockIdx.x % nblk);
   const int b = bh / p.Hq, h = bh % p.Hq;
+  // output row of query n: b*N + n, or start_q + n of sequence b
+  int len_q = p.N;
+  long long row0 = static_cast<long long>(b) * p.N;
+  if (VARLEN) {
+    int sq = 0, sk = 0, lk = 0;
+    if (!seq_span(p.vl, b, sq, len_q, sk, lk)) return;
+    if (n0 >= len_q) return;
+    row0 = sq;
+  }
   const float* src = p.dq_acc + static_cast<long long>(bh) * D * p.Npad + n0;
   for (int i = threadIdx.x; i < D * 64; i += 256) {
     const int dd = i >> 6, n = i & 63;
@@ -191,18 +248,18 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
   constexpr int G = D / 8;  // 8 outputs (16 B) per thread and step
   for (int i = threadIdx.x; i < 64 * G; i += 256) {
     const int n = i / G, g = i % G;
-    if (n0 + n >= p.N) continue;
+    if (n0 + n >= len_q) continue;
     uint4 o;
     o.x = bw_pack2<BF16>(tile[8 * g + 0][n] * p.scale, tile[8 * g + 1][n] * p.scale);
     o.y = bw_pack2<BF16>(tile[8 * g + 2][n] * p.scale, tile[8 * g + 3][n] * p.scale);
     o.z = bw_pack2<BF16>(tile[8 * g + 4][n] * p.scale, tile[8 * g + 5][n] * p.scale);
     o.w = bw_pack2<BF16>(tile[8 * g + 6][n] * p.scale, tile[8 * g + 7][n] * p.scale);
-    *reinterpret_cast<uint4*>(p.dq + ((static_cast<long long>(b) * p.N + n0 + n) * p.Hq + h) * D + 8 * g) = o;
+    *reinterpret_cast<uint4*>(p.dq + ((row0 + n0 + n) * p.Hq + h) * D + 8 * g) = o;
   }
 }
 
 // ------------------------------------------------------------------- main kernel
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_bwd[];
@@ -237,18 +294,41 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   // ---- work decode: key blocks of one (batch, key/value head) are consecutive CTAs
   // (ascending, so with the causal mask the heaviest come first); the CTAs resident
   // at any time then share a few heads' Q, dO and dQ accumulator through L2.
-  const int N = p.N;
+  const int N = VARLEN ? p.vl.max_k : p.N;  // key rows the grid covers per sequence
   const int nkb = (N + 127) / 128;
   const int jb = static_cast<int>(blockIdx.x % nkb);
   const int bhk = static_cast<int>(blockIdx.x / nkb);
   const int hkv = bhk % p.Hkv;
   const int b = bhk / p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int nqb = (N + 63) / 64;
-  const int qb0 = CAUSAL ? 2 * jb : 0;
-  const int nq = nqb - qb0;      // query blocks per head
-  const int T = G * nq;          // steps of this CTA
   const int k0 = 128 * jb;
+  // Sequence geometry (fixed length: len_q = len_k = N).  With variable lengths and the
+  // mask, query i sees key j iff j <= i + (len_k - len_q), so the first query block
+  // that sees key k0 is (k0 - off) / 64.
+  int start_q = 0, len_q = N, start_k = 0, len_k = N;
+  if (VARLEN) {
+    if (!seq_span(p.vl, b, start_q, len_q, start_k, len_k)) {
+      if (threadIdx.x == 0 && jb == 0 && hkv == 0) atomicOr(p.err, kDevErrSeqlens);
+      return;  // uniform, before any barrier or TMEM allocation
+    }
+    if (k0 >= len_k) return;
+  }
+  const int off = len_k - len_q;
+  const int nqb = (len_q + 63) / 64;
+  const int qb0 = CAUSAL ? (VARLEN ? max(0, k0 - off) / 64 : 2 * jb) : 0;
+  const int nq = max(0, nqb - qb0);  // query blocks per head
+  const int T = G * nq;              // steps of this CTA
+  if (VARLEN && T == 0) {
+    // no query sees these keys: dK = dV = 0
+    for (int i = threadIdx.x; i < 128 * (D / 8); i += blockDim.x) {
+      const int key = k0 + i / (D / 8);
+      if (key >= len_k) continue;
+      const long long o = (static_cast<long long>(start_k + key) * p.Hkv + hkv) * D + 8 * (i % (D / 8));
+      *reinterpret_cast<uint4*>(p.dk + o) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(p.dv + o) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -307,8 +387,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         tma_prefetch_desc(&p.tm_dq);
         mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
         for (int ch = 0; ch < C::CHUNKS; ++ch) {
-          tma_load_4d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, k0, b);
-          tma_load_4d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, k0, b);
+          if (VARLEN) {
+            tma_load_3d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, start_k + k0);
+            tma_load_3d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, start_k + k0);
+          } else {
+            tma_load_4d(sbase + C::OFF_K + ch * C::KV_CHUNK, &p.tm_k, kv_full, ch * 64, hkv, k0, b);
+            tma_load_4d(sbase + C::OFF_V + ch * C::KV_CHUNK, &p.tm_v, kv_full, ch * 64, hkv, k0, b);
+          }
         }
       }
       bool ok = true;
@@ -325,10 +410,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         if (leader) {
           mbar_arrive_expect_tx(st_full(s), 2 * C::Q_TILE + 2 * 256);
           for (int ch = 0; ch < C::CHUNKS; ++ch) {
-            tma_load_4d(sbase + C::OFF_Q + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_q, st_full(s), ch * 64, hq, q0,
-                        b);
-            tma_load_4d(sbase + C::OFF_DO + s * C::Q_TILE + ch * C::Q_CHUNK, &p.tm_do, st_full(s), ch * 64, hq,
-                        q0, b);
+            const uint32_t dq_ = sbase + C::OFF_Q + s * C::Q_TILE + ch * C::Q_CHUNK;
+            const uint32_t ddo = sbase + C::OFF_DO + s * C::Q_TILE + ch * C::Q_CHUNK;
+            if (VARLEN) {
+              tma_load_3d(dq_, &p.tm_q, st_full(s), ch * 64, hq, start_q + q0);
+              tma_load_3d(ddo, &p.tm_do, st_full(s), ch * 64, hq, start_q + q0);
+            } else {
+              tma_load_4d(dq_, &p.tm_q, st_full(s), ch * 64, hq, q0, b);
+              tma_load_4d(ddo, &p.tm_do, st_full(s), ch * 64, hq, q0, b);
+            }
           }
           const long long row = (static_cast<long long>(b) * p.Hq + hq) * p.Npad + q0;
           bulk_load(sbase + C::OFF_LD + s * 512, p.l2vec + row, 256, st_full(s));
@@ -501,8 +591,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       // same address in every lane)
       const float4* nl4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512) + cbase / 4;
       const float4* nd4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + s * 512 + 256) + cbase / 4;
-      // with the causal mask query column c sees this key iff c >= key - q0
-      const int cmin = CAUSAL ? key - q0 - cbase : 0;
+      // with the causal mask query column c sees this key iff c >= key - off - q0; with
+      // variable lengths a key past the sequence is seen by no column
+      const int cmin = (VARLEN && key >= len_k) ? (1 << 20) : (CAUSAL ? key - off - q0 - cbase : -(1 << 20));
       // the dS^T buffer of this parity must have been consumed by the MMAs of step it-2
       if (it >= 2 && !__all_sync(FULL, mbar_wait(ds_free(bb), ((it >> 1) - 1) & 1, abort_flag, lim))) {
         ok = false;
@@ -531,7 +622,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
           p1 = bw_ex2(p1);
           p2 = bw_ex2(p2);
           p3 = bw_ex2(p3);
-          if (CAUSAL) {
+          if (CAUSAL || VARLEN) {
             if (4 * c4 + 0 < cmin) p0 = 0.f;
             if (4 * c4 + 1 < cmin) p1 = 0.f;
             if (4 * c4 + 2 < cmin) p2 = 0.f;
@@ -574,13 +665,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       named_bar_sync_n(2, 128);
       if (wg_fail[0] == 0) {
         tc_fence_after();
-        uint16_t* out = p.dk + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
+        const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
+        uint16_t* out = p.dk + (krow * p.Hkv + hkv) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + lane_off + C::T_DK + 32u * c, v);
           tmem_wait_ld();
-          if (key < N) {
+          if (key < len_k) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               uint4 o;
@@ -660,13 +752,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     if (wg_fail[2] == 0) {
       tc_fence_after();
       const int key = k0 + r;
-      uint16_t* out = p.dv + ((static_cast<long long>(b) * N + key) * p.Hkv + hkv) * D;
+      const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
+      uint16_t* out = p.dv + (krow * p.Hkv + hkv) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::T_DV + 32u * c, v);
         tmem_wait_ld();
-        if (key < N) {
+        if (key < len_k) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 o;
@@ -689,44 +782,53 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long rows = static_cast<long long>(p.B) * p.N * p.Hq;
   {
+    // preprocess: LPR lanes per row, 8 rows per 256-thread block and step
+    const long long rows = VARLEN ? static_cast<long long>(p.B) * p.Hq * p.Npad : static_cast<long long>(p.B) * p.N * p.Hq;
     const long long want = (rows * (D / 8) + 255) / 256;
     const int grid = static_cast<int>(want < 8LL * sms ? (want > 0 ? want : 1) : 8LL * sms);
-    fa_bwd_preprocess<D, BF16><<<grid, 256, 0, stream>>>(p);
+    if (VARLEN)
+      fa_bwd_preprocess_varlen<D, BF16><<<grid, 256, 0, stream>>>(p);
+    else
+      fa_bwd_preprocess<D, BF16><<<grid, 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_main<D, BF16, CAUSAL>;
+    auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>((p.N + 127) / 128) * p.B * p.Hkv;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const long long nk = VARLEN ? p.vl.max_k : p.N;
+    const long long grid = ((nk + 127) / 128) * p.B * p.Hkv;
+    if (grid > 0) {
+      kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   {
-    const long long grid = static_cast<long long>(p.B) * p.Hq * ((p.N + 63) / 64);
-    fa_bwd_dq_convert<D, BF16><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+    const long long grid = static_cast<long long>(p.B) * p.Hq * (VARLEN ? p.Npad / 64 : (p.N + 63) / 64);
+    fa_bwd_dq_convert<D, BF16, VARLEN><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
     return cudaGetLastError();
   }
 }
 
-cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {
+template <int D, bool BF16>
+static cudaError_t launch_bwd_d(const BwdParams& p, bool causal, bool varlen, cudaStream_t stream) {
+  if (varlen) return causal ? launch_bwd_t<D, BF16, true, true>(p, stream) : launch_bwd_t<D, BF16, false, true>(p, stream);
+  return causal ? launch_bwd_t<D, BF16, true, false>(p, stream) : launch_bwd_t<D, BF16, false, false>(p, stream);
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream) {
   const bool bf = dtype == FA_BF16;
-  if (d == 128) {
-    if (bf) return causal ? launch_bwd_t<128, true, true>(p, stream) : launch_bwd_t<128, true, false>(p, stream);
-    return causal ? launch_bwd_t<128, false, true>(p, stream) : launch_bwd_t<128, false, false>(p, stream);
-  }
-  if (bf) return causal ? launch_bwd_t<64, true, true>(p, stream) : launch_bwd_t<64, true, false>(p, stream);
-  return causal ? launch_bwd_t<64, false, true>(p, stream) : launch_bwd_t<64, false, false>(p, stream);
+  if (d == 128) return bf ? launch_bwd_d<128, true>(p, causal, varlen, stream) : launch_bwd_d<128, false>(p, causal, varlen, stream);
+  return bf ? launch_bwd_d<64, true>(p, causal, varlen, stream) : launch_bwd_d<64, false>(p, causal, varlen, stream);
 }
 
 }  // namespace fa

@@ -64,7 +64,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
   // heads' K/V through L2.  With the causal mask tiles are issued heaviest first
   // (largest query offset) across all heads, which balances the last waves.
   // Consecutive heads of a GQA group share K/V in both orders.
-  const int N = p.N;
+  const int N = VARLEN ? p.vl.max_q : p.N;  // query rows the grid covers per sequence
   const int nqb = (N + 255) / 256;
   const int BH = p.B * p.Hq;
   int qb, bh;
@@ -107,11 +107,30 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;
   const int hkv = h / (p.Hq / p.Hkv);
-  const int nkb = (N + 127) / 128;
-  // query tile t covers rows [qb*256 + 128t, +128) and visits n_t key blocks
+  // Sequence geometry.  Fixed length: len_q = len_k = N.  Variable length: sequence b
+  // sits at rows [start, start + len) of the packed tensors, and with the causal mask
+  // query i sees key j iff j <= i + (len_k - len_q) (the mask is aligned at the
+  // bottom-right corner, so the last query sees every key).
+  int start_q = 0, len_q = N, start_k = 0, len_k = N;
+  if (VARLEN) {
+    if (!seq_span(p.vl, b, start_q, len_q, start_k, len_k)) {
+      if (threadIdx.x == 0 && qb == 0) atomicOr(p.err, kDevErrSeqlens);
+      return;  // uniform, before any barrier or TMEM allocation
+    }
+    if (qb * 256 >= len_q) return;
+  }
+  const int off = len_k - len_q;
+  // query tile t covers rows [qb*256 + 128t, +128) and visits n_t key blocks; with
+  // variable length the first nf_t of them need no mask for any row of the tile
   const int r00 = qb * 256, r01 = qb * 256 + 128;
-  const int n0 = CAUSAL ? (r00 / 128 + 1) : nkb;
-  const int n1 = (r01 >= N) ? 0 : (CAUSAL ? (r01 / 128 + 1) : nkb);
+  auto nblocks = [&](int r0) {
+    if (r0 >= len_q) return 0;
+    if (!VARLEN) return CAUSAL ? r0 / 128 + 1 : (N + 127) / 128;
+    const int ve = CAUSAL ? min(len_k, r0 + 128 + off) : len_k;  // keys seen by the tile's last row
+    return ve > 0 ? (ve + 127) / 128 : 0;
+  };
+  auto nfull = [&](int r0) { return max(0, CAUSAL ? min(len_k, r0 + off + 1) : len_k) / 128; };
+  const int n0 = nblocks(r00), n1 = nblocks(r01);
   auto n_of = [&](int t) { return t ? n1 : n0; };
   auto r0_of = [&](int t) { return t ? r01 : r00; };
   const int nmax = n0 > n1 ? n0 : n1;
@@ -161,9 +180,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       for (int t = 0; t < 2; ++t) {
         if (n_of(t) == 0) continue;
         mbar_arrive_expect_tx(q_full(t), C::TILE_BYTES);
-        for (int ch = 0; ch < C::CHUNKS; ++ch)
-          tma_load_4d(smem_u32(sQ + t * C::TILE_BYTES + ch * C::CHUNK_BYTES), &p.tm_q, q_full(t), ch * 64, h,
-                      r0_of(t), b);
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES + ch * C::CHUNK_BYTES);
+          if (VARLEN)
+            tma_load_3d(dst, &p.tm_q, q_full(t), ch * 64, h, start_q + r0_of(t));
+          else
+            tma_load_4d(dst, &p.tm_q, q_full(t), ch * 64, h, r0_of(t), b);
+        }
       }
     }
     int c = 0;
@@ -179,9 +202,13 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         if (leader) {
           mbar_arrive_expect_tx(kv_full(slot), C::TILE_BYTES);
           const CUtensorMap* map = kind ? &p.tm_v : &p.tm_k;
-          for (int ch = 0; ch < C::CHUNKS; ++ch)
-            tma_load_4d(smem_u32(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES), map, kv_full(slot), ch * 64,
-                        hkv, 128 * j, b);
+          for (int ch = 0; ch < C::CHUNKS; ++ch) {
+            const uint32_t dst = smem_u32(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES);
+            if (VARLEN)
+              tma_load_3d(dst, map, kv_full(slot), ch * 64, hkv, start_k + 128 * j);
+            else
+              tma_load_4d(dst, map, kv_full(slot), ch * 64, hkv, 128 * j, b);
+          }
         }
       }
     }
@@ -282,6 +309,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     const uint32_t o_tm = tbase + lane_off + 256u + uint32_t(D) * t;
     const float cl2 = p.scale_log2;
     const int row = r0_of(t) + rit;
+    const int nf = nfull(r0_of(t));
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_of(t); ++j) {
@@ -296,10 +324,11 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + 32u * c, sr + 32 * c);
       tmem_wait_ld();
       float* s = reinterpret_cast<float*>(sr);
-      if (j == n_of(t) - 1 && (CAUSAL || (N & 127))) {
-        // keys k0 + c are visible for c < nvis (key < N, and key <= row with the mask)
+      if (VARLEN ? j >= nf : (j == n_of(t) - 1 && (CAUSAL || (N & 127)))) {
+        // keys k0 + c are visible for c < nvis (key < len_k, and key <= row + off with
+        // the mask)
         const int k0 = 128 * j;
-        const int nvis = CAUSAL ? min(N, row + 1) - k0 : N - k0;
+        const int nvis = CAUSAL ? min(len_k, row + off + 1) - k0 : len_k - k0;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= nvis) s[c] = -INFINITY;
@@ -313,7 +342,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         // lazy correction: bring O and l to the new maximum (needs PV_t(j-1) done,
         // which the completion of S_t(j), issued after it, already implies)
         const float m_new = fmaxf(m, mx);
-        const float alpha = ex2f((m - m_new) * cl2);
+        // (a row that sees no key keeps m = -inf; its O and l stay 0)
+        const float alpha = (VARLEN && CAUSAL && m_new == -INFINITY) ? 1.f : ex2f((m - m_new) * cl2);
         m = m_new;
         l *= alpha;
 #pragma unroll
@@ -327,7 +357,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         tmem_wait_st();
       }
-      const float neg = -m * cl2;
+      // a row with no visible key so far (only possible with variable lengths and the
+      // mask) has m = -inf: its p are exp2(-inf) = 0
+      const float neg = (VARLEN && CAUSAL && m == -INFINITY) ? 0.f : -m * cl2;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
@@ -355,8 +387,12 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       named_bar_sync_n(1 + t, 128);
       if (wg_fail[t] == 0) {
         tc_fence_after();
-        // ---- epilogue: O / l -> 16-bit -> swizzled staging (Q_t's buffer) -> TMA store
-        const float inv = 1.0f / l;
+        // ---- epilogue: O / l -> 16-bit -> swizzled staging (Q_t's buffer) -> TMA store.
+        // A variable-length tile that ends past its sequence is written row by row
+        // instead (a tile store would run into the next sequence's rows).
+        const float inv = (VARLEN && CAUSAL) ? (l > 0.f ? 1.0f / l : 0.f) : 1.0f / l;
+        const bool direct = VARLEN && r0_of(t) + 128 > len_q;
+        uint16_t* orow = p.o + (static_cast<long long>(start_q + row) * p.Hq + h) * D;
         uint8_t* stage = sQ + t * C::TILE_BYTES;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -367,6 +403,15 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+          if (direct) {
+            if (row < len_q) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) =
+                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+            continue;
+          }
           uint8_t* rowp = stage + (c >> 1) * C::CHUNK_BYTES + rit * 128;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -375,15 +420,35 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
             *reinterpret_cast<uint4*>(rowp + phys * 16) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
-        fence_proxy_async_smem();
-        named_bar_sync_n(3 + t, 128);
-        if (rit == 0) {
-          for (int ch = 0; ch < C::CHUNKS; ++ch)
-            tma_store_4d(&p.tm_o, smem_u32(stage + ch * C::CHUNK_BYTES), ch * 64, h, r0_of(t), b);
-          bulk_commit_group();
-          bulk_wait_group0();
+        if (!direct) {  // uniform across the warpgroup
+          fence_proxy_async_smem();
+          named_bar_sync_n(3 + t, 128);
+          if (rit == 0) {
+            for (int ch = 0; ch < C::CHUNKS; ++ch) {
+              if (VARLEN)
+                tma_store_3d(&p.tm_o, smem_u32(stage + ch * C::CHUNK_BYTES), ch * 64, h, start_q + r0_of(t));
+              else
+                tma_store_4d(&p.tm_o, smem_u32(stage + ch * C::CHUNK_BYTES), ch * 64, h, r0_of(t), b);
+            }
+            bulk_commit_group();
+            bulk_wait_group0();
+          }
         }
-        if (row < N) p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] = m * p.scale + logf(l);
+        if (row < len_q) {
+          const float lse = (VARLEN && CAUSAL && !(l > 0.f)) ? -INFINITY : m * p.scale + logf(l);
+          if (VARLEN)
+            p.lse[static_cast<size_t>(h) * p.vl.total_q + start_q + row] = lse;
+          else
+            p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] = lse;
+        }
+      }
+    } else if (VARLEN && r0_of(t) < len_q) {
+      // no key is visible to any row of this tile: O = 0 and lse = ln 0 = -inf
+      if (row < len_q) {
+        uint16_t* orow = p.o + (static_cast<long long>(start_q + row) * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[static_cast<size_t>(h) * p.vl.total_q + start_q + row] = -INFINITY;
       }
     }
   }
@@ -396,26 +461,28 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long nqb = (p.N + 255) / 256;
+  const long long nqb = ((VARLEN ? p.vl.max_q : p.N) + 255) / 256;
   const long long grid = nqb * p.B * p.Hq;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {
+template <int D, bool BF16>
+static cudaError_t launch_fwd_d(const FwdParams& p, bool causal, bool varlen, cudaStream_t stream) {
+  if (varlen) return causal ? launch_fwd_t<D, BF16, true, true>(p, stream) : launch_fwd_t<D, BF16, false, true>(p, stream);
+  return causal ? launch_fwd_t<D, BF16, true, false>(p, stream) : launch_fwd_t<D, BF16, false, false>(p, stream);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream) {
   const bool bf = dtype == FA_BF16;
-  if (d == 128) {
-    if (bf) return causal ? launch_fwd_t<128, true, true>(p, stream) : launch_fwd_t<128, true, false>(p, stream);
-    return causal ? launch_fwd_t<128, false, true>(p, stream) : launch_fwd_t<128, false, false>(p, stream);
-  }
-  if (bf) return causal ? launch_fwd_t<64, true, true>(p, stream) : launch_fwd_t<64, true, false>(p, stream);
-  return causal ? launch_fwd_t<64, false, true>(p, stream) : launch_fwd_t<64, false, false>(p, stream);
+  if (d == 128) return bf ? launch_fwd_d<128, true>(p, causal, varlen, stream) : launch_fwd_d<128, false>(p, causal, varlen, stream);
+  return bf ? launch_fwd_d<64, true>(p, causal, varlen, stream) : launch_fwd_d<64, false>(p, causal, varlen, stream);
 }
 
 }  // namespace fa

@@ -14,25 +14,44 @@ namespace fa {
 // base misaligned (did no work).
 constexpr unsigned kDevErrTimeout = 1u;
 constexpr unsigned kDevErrLayout = 2u;
+// A variable-length launch found a sequence whose offsets or length contradict the
+// sizes it was given (it wrote nothing for that sequence).
+constexpr unsigned kDevErrSeqlens = 4u;
 
 // Bounded waits give up after this long (ns); a pipeline stage normally waits
 // microseconds, so only a broken pipeline gets near it.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Variable-length batches: sequence b owns rows [cu[b], cu[b+1]) of the packed
+// [total, H, d] tensors, of which the first len_b are real (len_b = used[b] when `used`
+// is given, else cu[b+1] - cu[b]).  Device pointers; all null for fixed-length calls.
+struct Seqlens {
+  const int* cu_q;
+  const int* cu_k;
+  const int* used_q;
+  const int* used_k;
+  int total_q, total_k;  // rows of the packed tensors
+  int max_q, max_k;      // upper bounds on len_b (size the grid)
+};
+
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 4-D maps over [B, N, H, d] (d innermost)
-  float* lse;                          // [B, Hq, N]
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // fixed: 4-D maps over [B, N, H, d]; varlen: 3-D over [total, H, d]
+  float* lse;                          // fixed: [B, Hq, N]; varlen: [Hq, total_q]
+  uint16_t* o;                         // varlen: rows of tiles that end past their sequence
   unsigned* err;                       // device error word
   int B, Hq, Hkv, N;
   float scale_log2;                    // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
+  Seqlens vl;
 };
 
 // Encodes a 4-D tensor map over a [B, N, H, d] 16-bit tensor, box = {64, 1, rows, 1},
 // 128-byte swizzle.  Returns false if the driver rejects it.
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
                      fa_dtype dtype);
+// 3-D map over a packed [total, H, d] 16-bit tensor, box = {64, 1, rows}, 128-byte swizzle.
+bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d, int box_rows, fa_dtype dtype);
 
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
@@ -48,9 +67,10 @@ struct BwdParams {
   float* dvec;              // workspace: -D = -rowsum(dO*O), [B*Hq, Npad] (0 past N)
   float* l2vec;             // workspace: -lse * log2(e), [B*Hq, Npad] (-inf past N)
   unsigned* err;
-  int B, Hq, Hkv, N, Npad;
+  int B, Hq, Hkv, N, Npad;  // varlen: N unused, Npad = max_q rounded up to 64 (at least 64)
   float scale, scale_log2;
   uint64_t wait_limit_ns;
+  Seqlens vl;  // varlen: packed layouts ([total, H, d] tensors, lse [Hq, total_q])
 };
 
 // Workspace layout for the backward pass (all offsets 256-byte aligned).
@@ -64,7 +84,22 @@ bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, in
 
 unsigned* device_error_word();  // address of this device's error word (device memory)
 
-cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
+
+// Geometry of sequence b of a variable-length launch; false if its offsets or length
+// contradict the launch's sizes.
+__device__ __forceinline__ bool seq_span(const Seqlens& vl, int b, int& start_q, int& len_q, int& start_k,
+                                         int& len_k) {
+  const int sq = vl.cu_q[b], eq = vl.cu_q[b + 1], sk = vl.cu_k[b], ek = vl.cu_k[b + 1];
+  const int lq = vl.used_q ? vl.used_q[b] : eq - sq;
+  const int lk = vl.used_k ? vl.used_k[b] : ek - sk;
+  start_q = sq;
+  len_q = lq;
+  start_k = sk;
+  len_k = lk;
+  return sq >= 0 && eq >= sq && eq <= vl.total_q && lq >= 0 && lq <= eq - sq && lq <= vl.max_q && sk >= 0 &&
+         ek >= sk && ek <= vl.total_k && lk >= 0 && lk <= ek - sk && lk <= vl.max_k;
+}
 
 }  // namespace fa

@@ -1,10 +1,11 @@
 """ctypes binding of libfa.so: argument marshalling only, every step runs in the library.
 
 The C names are mirrored one to one (``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``,
-``fa_check_device_error``, ``fa_status_string``).  ``forward`` / ``backward`` are
-conveniences that allocate the outputs with torch (device memory and streams are
-the only things torch provides here) and call the C entry points on the current
-stream.  Importing this module loads the library and raises if it is missing: there
+``fa_fwd_varlen``, ``fa_bwd_varlen``, ``fa_bwd_varlen_workspace_size``,
+``fa_check_device_error``, ``fa_status_string``).  ``forward`` / ``backward`` and
+``forward_varlen`` / ``backward_varlen`` are conveniences that allocate the outputs
+with torch (device memory and streams are the only things torch provides here) and
+call the C entry points on the current stream.  Importing this module loads the library and raises if it is missing: there
 is no fallback path.
 """
 
@@ -45,6 +46,12 @@ def _load():
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_fwd_varlen.argtypes = [vp] * 9 + [i] * 9 + [f, i, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd_varlen.argtypes = [vp] * 13 + [i] * 9 + [f, i, vp, sz, vp]
+    lib.fa_bwd_varlen.restype = i
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_check_device_error.argtypes = [vp]
@@ -83,6 +90,25 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, 
 
 def fa_bwd_workspace_size(B, Hq, Hkv, N, d) -> int:
     return int(lib.fa_bwd_workspace_size(B, Hq, Hkv, N, d))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, used_q, used_k, B, Hq, Hkv, total_q, total_k, max_q, max_k, d,
+                  causal, scale, dtype, stream) -> int:
+    """Mirror of the C ``fa_fwd_varlen``."""
+    return lib.fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, used_q, used_k, B, Hq, Hkv, total_q, total_k, max_q,
+                             max_k, d, int(causal), float(scale), int(dtype), stream)
+
+
+def fa_bwd_varlen_workspace_size(B, Hq, max_q, d) -> int:
+    return int(lib.fa_bwd_varlen_workspace_size(B, Hq, max_q, d))
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, used_q, used_k, B, Hq, Hkv, total_q, total_k,
+                  max_q, max_k, d, causal, scale, dtype, workspace, workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_bwd_varlen``."""
+    return lib.fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, used_q, used_k, B, Hq, Hkv, total_q,
+                             total_k, max_q, max_k, d, int(causal), float(scale), int(dtype), workspace,
+                             int(workspace_bytes), stream)
 
 
 def fa_selftest_wait_timeout(limit_us, stream) -> int:
@@ -148,6 +174,59 @@ def backward(dout, q, k, v, o, lse, causal=False, scale=None, workspace=None, dq
                 Hkv, N, d, causal, scale, _DT[q.dtype], _ptr(workspace), workspace.numel(), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def _varlen_shapes(q, k, v, cu_q, cu_k):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape != v.shape:
+        raise ValueError("varlen q must be [total_q, Hq, d], k and v [total_k, Hkv, d]")
+    if q.shape[2] != k.shape[2] or q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share d and a 16-bit dtype")
+    for t in (cu_q, cu_k):
+        if t.dtype != torch.int32 or t.dim() != 1 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous int32 CUDA vectors of B+1 offsets")
+    if cu_q.numel() != cu_k.numel() or cu_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B+1 >= 2 offsets")
+    return cu_q.numel() - 1, q.shape[0], k.shape[0], q.shape[1], k.shape[1], q.shape[2]
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
+                   seqused_q=None, seqused_k=None, out=None, lse=None, stream=None):
+    """Packed variable-length forward.  Returns (o [total_q,Hq,d], lse [Hq,total_q] fp32).
+
+    Rows outside every sequence are left as allocated (uninitialised unless `out` /
+    `lse` are passed in)."""
+    B, tq, tk, Hq, Hkv, d = _varlen_shapes(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                       _ptr(seqused_q), _ptr(seqused_k), B, Hq, Hkv, tq, tk, int(max_seqlen_q), int(max_seqlen_k), d,
+                       causal, scale, _DT[q.dtype], _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+    return o, lse
+
+
+def backward_varlen(dout, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
+                    scale=None, seqused_q=None, seqused_k=None, workspace=None, dq=None, dk=None, dv=None,
+                    stream=None):
+    """Packed variable-length backward.  Returns (dq, dk, dv); rows outside every
+    sequence are left as allocated."""
+    B, tq, tk, Hq, Hkv, d = _varlen_shapes(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ws_bytes = fa_bwd_varlen_workspace_size(B, Hq, int(max_seqlen_q), d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(seqused_q), _ptr(seqused_k), B, Hq, Hkv, tq, tk,
+                       int(max_seqlen_q), int(max_seqlen_k), d, causal, scale, _DT[q.dtype], _ptr(workspace),
+                       workspace.numel(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
     return dq, dk, dv
 
 

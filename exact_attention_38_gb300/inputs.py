@@ -45,3 +45,26 @@ def make_inputs(B, N, Hq, Hkv, d, dtype="bf16", seed=0, with_do=True, special=No
 def to_f64(t):
     """Exact upcast of a 16-bit CPU tensor to a float64 numpy array."""
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make_varlen_inputs(seg_q, seg_k, Hq, Hkv, d, dtype="bf16", seed=0):
+    """Packed variable-length batch: CPU tensors q, do [sum(seg_q), Hq, d] and k, v
+    [sum(seg_k), Hkv, d] (16-bit ``dtype``) and int32 offsets cu_q, cu_k [B+1].
+
+    ``seg_q[b]`` / ``seg_k[b]`` are the rows each sequence owns in the packed tensors
+    (its length, or for a padded batch its padded length).  Same draw recipe as
+    ``make_inputs``: one CPU generator, fp32 normals for q, k, v, dO in that order,
+    rounded to nearest into the 16-bit type.
+    """
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    tq, tk = int(sum(seg_q)), int(sum(seg_k))
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((tq, Hq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((tk, Hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((tk, Hkv, d), generator=g, dtype=torch.float32)
+    do = torch.randn((tq, Hq, d), generator=g, dtype=torch.float32)
+    cu_q = torch.zeros(len(seg_q) + 1, dtype=torch.int32)
+    cu_k = torch.zeros(len(seg_k) + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.tensor(list(seg_q), dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.tensor(list(seg_k), dtype=torch.int64), 0).to(torch.int32)
+    return {"q": q.to(tdt), "k": k.to(tdt), "v": v.to(tdt), "do": do.to(tdt), "cu_q": cu_q, "cu_k": cu_k}

@@ -102,6 +102,67 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_stream_t stream);
 
 /*
+ * Variable-length batches and unequal query / key lengths
+ * ------------------------------------------------------
+ * Several sequences packed along the token axis, each with its own query length
+ * len_q(b) and key length len_k(b).  The pages name boundary handling as a cost of the
+ * method ("FlashAttention-2: atención eficiente en GPU para contextos largos", section
+ * "Tres mejoras en la utilización de la GPU") and distinguish prefill from decode
+ * (section "Cómo documentar una diferencia técnica"); they give no interface, so this
+ * one is a reading:
+ *  - Layouts (packed, contiguous): q, o, dq, dout [total_q, Hq, d]; k, v, dk, dv
+ *    [total_k, Hkv, d] (dtype); lse [Hq, total_q] fp32.
+ *  - cu_seqlens_q / cu_seqlens_k: DEVICE int32 arrays of B+1 offsets.  Sequence b owns
+ *    rows [cu[b], cu[b+1]).  seqused_q / seqused_k: optional DEVICE int32 arrays of B
+ *    lengths (NULL = none).  When given, only the first seqused[b] rows of the segment
+ *    are real.  This serves padded batches: cu[b] = b * Nmax with the true lengths in
+ *    seqused.
+ *  - len(b) = seqused[b] if given, else cu[b+1] - cu[b]; every len(b) must be <= the
+ *    max_seqlen_* given (which sizes the grid).  Length 0 is allowed.
+ *  - Causal mask aligned at the BOTTOM-RIGHT corner: query i of sequence b sees key j
+ *    iff j <= i + len_k(b) - len_q(b), so the last query sees every key (with equal
+ *    lengths this is the usual j <= i).  A query that sees no key (len_k = 0, or
+ *    i < len_q - len_k under the mask) gets o = 0, lse = -inf, and zero gradients.
+ *  - Rows that belong to no sequence (the padding past seqused, gaps between
+ *    segments) are not written by any call.
+ *  - The offsets and lengths are read by the kernels, not on the host.  A sequence
+ *    whose values contradict total_* / max_seqlen_* (negative length, segment past the
+ *    end, length above the maximum, decreasing offsets) is skipped, and the next
+ *    fa_check_device_error() returns FA_ERR_INVALID.
+ *  - Pointers: 16-byte aligned as above, except that the tensors of a side whose
+ *    total is 0 are not read or written and may be NULL; offset arrays 4-byte aligned.
+ */
+
+/*
+ * Forward pass over a variable-length batch (see above).  total_q / total_k: rows of
+ * the packed tensors; max_seqlen_q / max_seqlen_k: bounds on the lengths.  Other
+ * arguments as fa_fwd.  total_q == 0 enqueues nothing.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, const int* seqused_q, const int* seqused_k, int B, int Hq,
+                        int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal,
+                        float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Workspace bytes for fa_bwd_varlen: the fa_bwd layout with N replaced by
+ * max_seqlen_q (Npad = max_seqlen_q rounded up to 64, at least 64), i.e. an fp32 dQ
+ * accumulator [B*Hq, d, Npad] plus two [B*Hq, Npad] fp32 vectors.  0 for invalid sizes.
+ */
+size_t fa_bwd_varlen_workspace_size(int B, int Hq, int max_seqlen_q, int d);
+
+/*
+ * Backward pass over a variable-length batch: gradients of L = sum(dout * o) for the
+ * rows of every sequence; o and lse from fa_fwd_varlen with the same inputs.  dq, dk
+ * and dv rows of each sequence are overwritten; other rows are left as they are.
+ * workspace as for fa_bwd, sized by fa_bwd_varlen_workspace_size().
+ */
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, const int* seqused_q, const int* seqused_k, int B, int Hq, int Hkv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale,
+                        fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
@@ -136,7 +197,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 /*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting and wound down without
- * finishing its work; its outputs are undefined) or FA_ERR_CUDA (a CUDA call failed,
+ * finishing its work; its outputs are undefined), FA_ERR_INVALID (a variable-length
+ * call found inconsistent sequence offsets or lengths) or FA_ERR_CUDA (a CUDA call failed,
  * or a kernel found its launch unusable, e.g. a misaligned shared-memory base, and did
  * no work).
  */

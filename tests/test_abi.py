@@ -103,3 +103,65 @@ def test_workspace_size(lib):
 ])
 def test_bwd_argument_errors_need_no_device(lib, kw, code):
     assert _bwd(lib, **kw) == code
+
+
+def _fwd_varlen(lib, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, cu_q=0x60000, cu_k=0x70000, used_q=None,
+             used_k=None, B=3, Hq=4, Hkv=2, total_q=300, total_k=500, max_q=200, max_k=300, d=128, causal=1,
+             scale=0.088, dtype=0)
+    a.update(kw)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f = lib.fa_fwd_varlen
+    f.argtypes = [vp] * 9 + [i] * 9 + [ctypes.c_float, i, vp]
+    f.restype = i
+    return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu_q"], a["cu_k"], a["used_q"], a["used_k"], a["B"],
+             a["Hq"], a["Hkv"], a["total_q"], a["total_k"], a["max_q"], a["max_k"], a["d"], a["causal"],
+             a["scale"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_q=None), 1), (dict(cu_k=0x70002), 1), (dict(used_q=0x80001), 1), (dict(q=0x10008), 1),
+    (dict(total_q=-1), 1), (dict(max_k=-3), 1), (dict(B=0), 1), (dict(Hq=3), 1), (dict(scale=0.0), 1),
+    (dict(d=96), 2), (dict(max_q=(1 << 20) + 1), 2),
+    (dict(total_q=0, q=None, o=None, lse=None), 0),  # no query row: nothing is enqueued
+])
+def test_fwd_varlen_argument_errors_need_no_device(lib, kw, code):
+    assert _fwd_varlen(lib, **kw) == code
+
+
+def _bwd_varlen(lib, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, do=0x60000, dq=0x70000, dk=0x80000,
+             dv=0x90000, cu_q=0xa0000, cu_k=0xb0000, used_q=None, used_k=None, B=3, Hq=4, Hkv=2, total_q=300,
+             total_k=500, max_q=200, max_k=300, d=64, causal=0, scale=0.125, dtype=1, ws=0x100000, ws_bytes=None)
+    a.update(kw)
+    lib.fa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_varlen_workspace_size.argtypes = [ctypes.c_int] * 4
+    need = lib.fa_bwd_varlen_workspace_size(a["B"], a["Hq"], a["max_q"], a["d"])
+    ws_bytes = need if a["ws_bytes"] is None else a["ws_bytes"]
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f = lib.fa_bwd_varlen
+    f.argtypes = [vp] * 13 + [i] * 9 + [ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+    f.restype = i
+    return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["cu_q"], a["cu_k"],
+             a["used_q"], a["used_k"], a["B"], a["Hq"], a["Hkv"], a["total_q"], a["total_k"], a["max_q"], a["max_k"],
+             a["d"], a["causal"], a["scale"], a["dtype"], a["ws"], ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(do=None), 1), (dict(dk=0x80004), 1), (dict(cu_q=None), 1), (dict(ws=None), 1), (dict(ws_bytes=4096), 1),
+    (dict(Hkv=3), 1), (dict(d=80), 2), (dict(total_k=-2), 1),
+    (dict(total_q=0, total_k=0, q=None, k=None, v=None, o=None, lse=None, do=None, dq=None, dk=None, dv=None), 0),
+])
+def test_bwd_varlen_argument_errors_need_no_device(lib, kw, code):
+    assert _bwd_varlen(lib, **kw) == code
+
+
+def test_varlen_workspace_size(lib):
+    lib.fa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_varlen_workspace_size.argtypes = [ctypes.c_int] * 4
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 5
+    # the fixed-length layout with N = max_seqlen_q (at least one 64-row block)
+    assert lib.fa_bwd_varlen_workspace_size(3, 4, 200, 128) == lib.fa_bwd_workspace_size(3, 4, 4, 200, 128)
+    assert lib.fa_bwd_varlen_workspace_size(3, 4, 0, 128) == lib.fa_bwd_workspace_size(3, 4, 4, 64, 128)
+    assert lib.fa_bwd_varlen_workspace_size(3, 4, 10, 96) == 0
