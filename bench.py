@@ -47,6 +47,11 @@ def parse():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--varlen", action="store_true",
+                    help="packed variable-length batch of --N tokens (default 16384): sequence lengths drawn "
+                         "uniformly from [--min-len, --max-len] with a fixed seed")
+    ap.add_argument("--min-len", type=int, default=512)
+    ap.add_argument("--max-len", type=int, default=4096)
     return ap.parse_args()
 
 
@@ -377,10 +382,121 @@ def run_native(a):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- variable-length batches
+
+def varlen_lengths(total, lo, hi, seed=7):
+    """Sequence lengths drawn uniformly from [lo, hi] (Python's seeded generator) until
+    `total` tokens are reached; the last one is cut to fit."""
+    import random
+
+    rng = random.Random(seed)
+    lens = []
+    while sum(lens) < total:
+        lens.append(rng.randint(lo, hi))
+    lens[-1] -= sum(lens) - total
+    return [n for n in lens if n > 0]
+
+
+def visible_pairs(nq, nk, causal):
+    """(query, key) pairs the mask leaves visible; the mask is aligned at the
+    bottom-right corner (query i sees key j iff j <= i + nk - nq)."""
+    if not causal:
+        return nq * nk
+    return sum(max(0, min(nk, i + nk - nq + 1)) for i in range(nq))
+
+
+def run_varlen(a):
+    import torch
+
+    from exact_attention_38_gb300 import fa
+    from exact_attention_38_gb300.inputs import make_varlen_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    total = a.N
+    lens = varlen_lengths(total, a.min_len, a.max_len)
+    Hq = a.H
+    Hkv = a.Hkv if a.Hkv is not None else a.H
+    d, causal = a.d, bool(a.causal)
+    x = make_varlen_inputs(lens, lens, Hq, Hkv, d, dtype="bf16", seed=3)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = x["cu_q"].to(dev)
+    mx = max(lens)
+    scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_varlen_workspace_size(len(lens), Hq, mx, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    B = len(lens)
+
+    def fwd():
+        st = fa.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), cu.data_ptr(),
+                              cu.data_ptr(), None, None, B, Hq, Hkv, total, total, mx, mx, d, causal, scale,
+                              fa.FA_BF16, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_varlen")
+
+    def bwd():
+        st = fa.fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu.data_ptr(), cu.data_ptr(), None, None,
+                              B, Hq, Hkv, total, total, mx, mx, d, causal, scale, fa.FA_BF16, ws.data_ptr(),
+                              ws_bytes, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd_varlen")
+
+    for _ in range(a.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+          for n in ("fwd", "bwd")}
+    stream = torch.cuda.current_stream(dev)
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        for i in range(a.steps):
+            flush.zero_()
+            for n, fn in (("fwd", fwd), ("bwd", bwd)):
+                ev[n][i][0].record(stream)
+                fn()
+                ev[n][i][1].record(stream)
+        torch.cuda.synchronize()
+    fa.check_device_error()
+    ms = {n: statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev[n]) for n in ev}
+    f_fwd = sum(4.0 * Hq * d * visible_pairs(n, n, causal) for n in lens)
+    fl = {"fwd": f_fwd, "bwd": 2.5 * f_fwd}
+    peak_tf, _, peak_kind = measured_peaks()
+    passes = {n: {"ms": ms[n], "tflops": fl[n] / (ms[n] * 1e-3) / 1e12} for n in ms}
+    for n in passes:
+        passes[n]["frac_of_peak"] = passes[n]["tflops"] / peak_tf
+    ms_step = ms["fwd"] + ms["bwd"]
+    value = (fl["fwd"] + fl["bwd"]) / (ms_step * 1e-3) / 1e12
+    dom = max(ms, key=ms.get)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"exact attention fwd+bwd, packed variable-length batch of {total} tokens: "
+                                   f"{B} sequences, lengths uniform in [{a.min_len}, {a.max_len}] (seed 7), "
+                                   f"Hq={Hq} Hkv={Hkv} d={d} bf16 {'causal' if causal else 'non-causal'}",
+                       "lengths": lens, "l2": "flushed between steps (outside the timed events)"},
+            "passes": passes,
+            "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel" if dom == "fwd" else "fa_bwd_main",
+                         "achieved": passes[dom]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": passes[dom]["tflops"] / peak_tf, "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 dense, burst (of measured)"},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": 4 * a.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.varlen:
+        run_varlen(a)
     else:
         run_native(a)
 
