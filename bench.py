@@ -50,6 +50,11 @@ def parse():
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length batch of --N tokens (default 16384): sequence lengths drawn "
                          "uniformly from [--min-len, --max-len] with a fixed seed")
+    ap.add_argument("--decode", action="store_true",
+                    help="decode forward: --B sequences (default 8) of --N cached keys (default 16384), "
+                         "--Nq new queries, Hq=--H (default 32 here), Hkv=--Hkv (default 8 here)")
+    ap.add_argument("--Nq", type=int, default=1)
+    ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--min-len", type=int, default=512)
     ap.add_argument("--max-len", type=int, default=4096)
     return ap.parse_args()
@@ -491,10 +496,81 @@ def run_varlen(a):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(a):
+    import torch
+
+    from exact_attention_38_gb300 import fa
+    from exact_attention_38_gb300.inputs import make_decode_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    B = a.B if a.B is not None else 8
+    Hq = a.H if a.H != 16 else 32  # the GQA shape of the long-context configuration by default
+    Hkv = a.Hkv if a.Hkv is not None else 8
+    N, Nq, d, causal = a.N, a.Nq, a.d, bool(a.causal)
+    x = make_decode_inputs(B, Nq, N, Hq, Hkv, d, dtype="bf16", seed=3)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    cl = torch.full((B,), N, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    S = fa.fa_decode_num_splits(B, Hq, Hkv, Nq, N, d, a.splits)
+    ws_bytes = fa.fa_decode_workspace_size(B, Hq, Hkv, Nq, N, d, a.splits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    scale = 1.0 / math.sqrt(d)
+
+    def step():
+        st = fa.fa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), cl.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, Hq, Hkv, Nq, N, d, causal, scale, a.splits, fa.FA_BF16, ws.data_ptr(), ws_bytes, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_decode")
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        for i in range(a.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    fa.check_device_error()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    # algorithmic bytes: every cached key and value row once, q read, o and lse written
+    kv_bytes = 2 * B * N * Hkv * d * 2
+    io_bytes = 2 * B * Nq * Hq * d * 2 + 4 * B * Hq * Nq
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    _, peak_hbm, peak_kind = measured_peaks()
+    pairs = sum(visible_pairs(Nq, N, causal) for _ in range(B))
+    tflops = 4.0 * Hq * d * pairs / (ms * 1e-3) / 1e12
+    line = {"metric": "decode: KV-cache bytes read per second", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"exact attention decode forward: B={B} sequences x {N} cached keys, Nq={Nq} new "
+                                   f"queries, Hq={Hq} Hkv={Hkv} d={d} bf16 {'causal' if causal else 'non-causal'}, "
+                                   f"{S} key splits",
+                       "l2": "flushed between steps (outside the timed events); the cache exceeds L2"},
+            "tflops": tflops,
+            "roofline": {"bound": "hbm", "kernel": "fa_decode_kernel (+ fa_decode_combine)", "achieved": gbs,
+                         "peak": peak_hbm, "unit": "GB/s", "frac": gbs / peak_hbm, "traffic": None,
+                         "bytes_per_step": kv_bytes + io_bytes, "peak_kind": f"{peak_kind} HBM copy (of measured)"},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": (2 if S > 1 else 1) * a.steps,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.decode:
+        run_decode(a)
     elif a.varlen:
         run_varlen(a)
     else:

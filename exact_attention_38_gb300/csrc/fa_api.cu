@@ -76,6 +76,52 @@ fa_status check_varlen(int B, int Hq, int Hkv, int total_q, int total_k, int max
 
 bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// Split count of the decode pass: enough CTAs for about four per SM slot on a 152-SM
+// part at two CTAs per SM (a fixed target, so the workspace size does not depend on the
+// device), never more splits than key blocks; `want` > 0 overrides the target.
+struct DecodeSplit {
+  int S, cps;
+};
+DecodeSplit decode_split(int B, int Hkv, int Nmax, int want) {
+  const int nkb = (Nmax + 127) / 128;
+  const long long units = static_cast<long long>(B) * Hkv;
+  long long S = want > 0 ? want : (1216 + units - 1) / units;
+  if (S > nkb) S = nkb;
+  if (S < 1) S = 1;
+  const int cps = static_cast<int>((nkb + S - 1) / S);
+  return {static_cast<int>((nkb + cps - 1) / cps), cps};
+}
+
+fa_status check_decode(int B, int Hq, int Hkv, int Nq, int Nmax, int d, float scale, int dtype, int num_splits) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nmax < 1 || d < 1 || num_splits < 0) return FA_ERR_INVALID;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((Hq / Hkv) * Nq > 128) return FA_ERR_UNSUPPORTED;  // the group's rows fill one 128-row tile
+  if (Nmax > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  const long long kv = static_cast<long long>(B) * Nmax * Hkv * d * 2;
+  if (kv >= (1LL << 40) || static_cast<long long>(B) * Nq * Hq * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * decode_split(B, Hkv, Nmax, num_splits).S >= (1LL << 31))
+    return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+struct DecodeWorkspace {
+  size_t opart_off, lpart_off, total;
+};
+DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  DecodeWorkspace w{};
+  if (sp.S == 1) return w;
+  const size_t rows = static_cast<size_t>(B) * Hkv * sp.S * (Hq / Hkv) * Nq;
+  w.opart_off = 0;
+  w.lpart_off = up(rows * d * 4);
+  w.total = w.lpart_off + up(rows * 4);
+  return w;
+}
+
 }  // namespace
 
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d) {
@@ -103,6 +149,11 @@ unsigned* device_error_word() {
 
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
                      fa_dtype dtype) {
+  return encode_bshd_box_map(map, base, B, N, H, d, 1, box_rows, dtype);
+}
+
+bool encode_bshd_box_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_h, int box_rows,
+                         fa_dtype dtype) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
@@ -110,7 +161,7 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   const cuuint64_t es = 2;
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(H) * d * es,
                                  static_cast<cuuint64_t>(N) * H * d * es};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_h), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r =
       enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -340,6 +391,60 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   p.wait_limit_ns = kWaitLimitNs;
   p.vl = Seqlens{cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, total_q, total_k, max_seqlen_q, max_seqlen_k};
   const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, true, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits) {
+  if (check_decode(B, Hq, Hkv, Nq, Nmax, d, 1.0f, FA_BF16, num_splits) != FA_OK) return 0;
+  return decode_workspace_layout(B, Hq, Hkv, Nq, Nmax, d, num_splits).total;
+}
+
+int fa_decode_num_splits(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits) {
+  if (check_decode(B, Hq, Hkv, Nq, Nmax, d, 1.0f, FA_BF16, num_splits) != FA_OK) return 0;
+  return decode_split(B, Hkv, Nmax, num_splits).S;
+}
+
+fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache, const int* cache_seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Nq, int Nmax, int d, int causal, float scale,
+                        int num_splits, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                        fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID;
+  if (!aligned4(cache_seqlens)) return FA_ERR_INVALID;
+  const fa_status st = check_decode(B, Hq, Hkv, Nq, Nmax, d, scale, static_cast<int>(dtype), num_splits);
+  if (st != FA_OK) return st;
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, Nq, Nmax, d, num_splits);
+  if (ws.total > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                       workspace_bytes < ws.total))
+    return FA_ERR_INVALID;
+  const int G = Hq / Hkv;
+  DecParams p{};
+  if (!encode_bshd_box_map(&p.tm_q, q, B, Nq, Hq, d, G, Nq, dtype) ||
+      !encode_bshd_map(&p.tm_k, k_cache, B, Nmax, Hkv, d, 128, dtype) ||
+      !encode_bshd_map(&p.tm_v, v_cache, B, Nmax, Hkv, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  p.seqlens_k = cache_seqlens;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.opart = ws.total ? reinterpret_cast<float*>(w + ws.opart_off) : nullptr;
+  p.lpart = ws.total ? reinterpret_cast<float*>(w + ws.lpart_off) : nullptr;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nmax = Nmax;
+  p.G = G;
+  p.M = G * Nq;
+  p.S = sp.S;
+  p.cps = sp.cps;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_decode(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

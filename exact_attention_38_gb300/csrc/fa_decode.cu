@@ -1,0 +1,476 @@
+// Decode-shaped forward with the key range split across CTAs (split-KV).
+//
+// A few new queries per sequence (Nq, the tokens being generated) attend to a long
+// key/value cache.  The pages separate this decode regime from prefill
+// ("FlashAttention-2: atención eficiente en GPU para contextos largos", section "Cómo
+// documentar una diferencia técnica") and motivate splitting work along the sequence
+// when batch and heads alone leave the GPU idle (section "Tres mejoras en la
+// utilización de la GPU"); the method is still exact attention.
+//
+// GB300 form:
+//  * one CTA per (batch, key/value head, key split); the G = Hq/Hkv query heads of the
+//    group and the Nq queries are packed into the rows of one 128-row tile (row
+//    r = i*G + g), loaded by a single TMA box, so every key/value block read from HBM
+//    serves the whole group;
+//  * the same tcgen05 pipeline as the prefill kernel for that one tile: a TMA warp
+//    streams K_j / V_j through a ring, an MMA warp issues S = Q K^T and O += P V with P
+//    read from tensor memory, and one softmax warpgroup keeps m and l per row;
+//  * each split writes its normalised partial output and log-sum-exp (fp32), and a
+//    combine kernel merges the splits: lse = ln sum_s e^{lse_s},
+//    O = sum_s e^{lse_s - lse} O_s.  With one split the kernel writes O and lse itself;
+//  * two CTAs per SM (256 threads, 256 TMEM columns and < 100 KB shared memory each),
+//    so the two CTAs' K/V streams overlap each other's serial softmax / MMA chain
+//    (the softmax warpgroup runs with 176 registers, the control warps with 80);
+//    the pass is bound by the HBM bytes of the cache.
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace fa {
+
+template <int D>
+struct DecCfg {
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile, or one K / V block of 128 keys
+  static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int THREADS = 256;             // softmax warpgroup + control warpgroup
+  static constexpr int NBARS = 4 + 2 * STAGES + 1;
+  static constexpr int SMEM = 1024 + (1 + STAGES) * TILE_BYTES + 8 * NBARS + 64;
+  static constexpr uint32_t TMEM_COLS = 256;      // S (128) and O (D <= 128)
+  static_assert(2 * SMEM <= 232448, "two CTAs per SM");
+};
+
+__device__ __forceinline__ float dec_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t dec_pack2(float lo, float hi) {
+  uint32_t r;
+  if (BF16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Writes the result of a row that sees no key (o = 0, lse = -inf), or of an empty
+// split (partial o = 0, partial lse = -inf: weight 0 in the combine).
+template <int D>
+__device__ __forceinline__ void dec_write_empty_row(const DecParams& p, int b, int hkv, int s, int r) {
+  if (p.S == 1) {
+    const int i = r / p.G, h = hkv * p.G + r % p.G;
+    uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D;
+    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0u, 0u, 0u, 0u);
+    p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = -INFINITY;
+  } else {
+    const long long prow = (static_cast<long long>(b * p.Hkv + hkv) * p.S + s) * p.M + r;
+    float4* orow = reinterpret_cast<float4*>(p.opart + prow * D);
+    for (int c = 0; c < D / 4; ++c) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    p.lpart[prow] = -INFINITY;
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DecCfg<D>;
+  extern __shared__ uint8_t smem_raw_dec[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_dec) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::STAGES * C::TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0, s_full = bar0 + 8u, p_full = bar0 + 16u, o_done = bar0 + 24u;
+  auto kv_full = [&](int st) { return bar0 + 8u * (4 + st); };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (4 + C::STAGES + st); };
+  const uint32_t final_bar = bar0 + 8u * (4 + 2 * C::STAGES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work decode: CTA = (batch, kv head, split); splits of one (b, kv head) are
+  // consecutive CTAs
+  const int s = static_cast<int>(blockIdx.x % p.S);
+  const int bh = static_cast<int>(blockIdx.x / p.S);
+  const int hkv = bh % p.Hkv;
+  const int b = bh / p.Hkv;
+  const int len_k = p.seqlens_k[b];
+  if (len_k < 0 || len_k > p.Nmax) {
+    if (threadIdx.x == 0 && s == 0 && hkv == 0) atomicOr(p.err, kDevErrSeqlens);
+    return;  // uniform, before any barrier
+  }
+  const int nkb = (len_k + 127) / 128;
+  const int jb0 = s * p.cps;
+  const int n = max(0, min(nkb, jb0 + p.cps) - jb0);  // key blocks of this split
+  // query i (row r = i*G + g) sees key j iff j < len_k and, with the mask, j <= i + off
+  const int off = len_k - p.Nq;
+  const int lim0 = CAUSAL ? max(0, min(len_k, off + 1)) : len_k;  // keys seen by query 0
+  const int nfull = lim0 / 128;  // blocks every row sees completely
+  if (n == 0) {
+    for (int r = threadIdx.x; r < p.M; r += blockDim.x) dec_write_empty_row<D>(p, b, hkv, s, r);
+    return;
+  }
+
+  // rows [M, 128) of the query tile are not written by the copy: zero them so every
+  // row the tensor core reads is finite
+  if (p.M < 128) {
+    for (int i = threadIdx.x; i < C::CHUNKS * (128 - p.M) * 8; i += blockDim.x) {
+      const int ch = i / ((128 - p.M) * 8), rem = i % ((128 - p.M) * 8);
+      *reinterpret_cast<uint4*>(sQ + ch * C::CHUNK_BYTES + (p.M + rem / 8) * 128 + (rem % 8) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *wg_fail = 0;
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(kv_full(st), 1);
+      mbar_init(kv_empty(st), 1);
+    }
+    mbar_init(final_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint64_t lim = p.wait_limit_ns;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(p.err, kDevErrTimeout);
+  };
+  constexpr unsigned FULL = 0xffffffffu;
+
+  if (warp >= 4) {
+    setmaxnreg_dec<80>();
+    const bool leader = elect_one();
+    if (warp == 4) {
+      // ------------------------------------------------------------ TMA producer
+      if (leader) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        // the group's query heads x the new queries: one box per 64-column chunk
+        mbar_arrive_expect_tx(q_full, C::CHUNKS * p.M * 128);
+        for (int ch = 0; ch < C::CHUNKS; ++ch)
+          tma_load_4d(smem_u32(sQ + ch * C::CHUNK_BYTES), &p.tm_q, q_full, ch * 64, hkv * p.G, 0, b);
+      }
+      int c = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind, ++c) {
+          const int slot = c % C::STAGES;
+          if (c >= C::STAGES &&
+              !__all_sync(FULL, mbar_wait(kv_empty(slot), ((c / C::STAGES) - 1) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(kv_full(slot), C::TILE_BYTES);
+            const CUtensorMap* map = kind ? &p.tm_v : &p.tm_k;
+            for (int ch = 0; ch < C::CHUNKS; ++ch)
+              tma_load_4d(smem_u32(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES), map, kv_full(slot), ch * 64,
+                          hkv, 128 * (jb0 + j), b);
+          }
+        }
+      }
+      if (!ok) {
+        if (leader) fail();
+        for (int i = (c > C::STAGES ? c - C::STAGES : 0); i < c; ++i)
+          mbar_wait(kv_full(i % C::STAGES), (i / C::STAGES) & 1, nullptr, lim);
+        mbar_wait(q_full, 0, nullptr, lim);
+      }
+      __syncwarp();
+    } else if (warp == 5) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+      constexpr uint32_t id_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+      bool ok = __all_sync(FULL, mbar_wait(q_full, 0, abort_flag, lim));
+      const uint32_t s_tm = tbase, o_tm = tbase + 128u;
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dkv0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::CHUNK_BYTES, 1024);
+      for (int j = 0; j <= n && ok; ++j) {
+        const int kc = 2 * j, vc = 2 * j - 1;
+        const int kslot = kc % C::STAGES, vslot = (vc + C::STAGES) % C::STAGES;
+        if (j < n && !__all_sync(FULL, mbar_wait(kv_full(kslot), (kc / C::STAGES) & 1, abort_flag, lim))) {
+          ok = false;
+          break;
+        }
+        if (j > 0) {
+          if (!__all_sync(FULL, mbar_wait(kv_full(vslot), (vc / C::STAGES) & 1, abort_flag, lim) &&
+                                    mbar_wait(p_full, (j - 1) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O += P(j-1) V_{j-1}: P from TMEM over S's columns, V MN-major
+          const uint64_t vd = dv0 + static_cast<uint64_t>((vslot * C::TILE_BYTES) >> 4);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(o_tm, s_tm + 8u * kk, vd + static_cast<uint64_t>((kk * 2048) >> 4), id_pv,
+                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            if (j == n) mma_commit(o_done);
+          }
+        }
+        tc_fence_after();
+        if (j < n) {
+          // S = Q K_j^T (in issue order after the product above, which read P from the
+          // same columns)
+          const uint64_t kd = dkv0 + static_cast<uint64_t>((kslot * C::TILE_BYTES) >> 4);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t o16 = static_cast<uint64_t>(((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4);
+              mma_ss(s_tm, dq0 + o16, kd + o16, id_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full);
+          }
+        }
+        if (leader) {
+          if (j > 0) mma_commit(kv_empty(vslot));
+          if (j < n) mma_commit(kv_empty(kslot));
+        }
+      }
+      if (!ok && leader) fail();
+      if (leader) mma_commit(final_bar);
+      mbar_wait(final_bar, 0, nullptr, lim);
+      // the last commits to kv_empty have no consumer: let them land before exit
+      if (ok) {
+        for (int c = (2 * n > C::STAGES ? 2 * n - C::STAGES : 0); c < 2 * n; ++c)
+          mbar_wait(kv_empty(c % C::STAGES), (c / C::STAGES) & 1, nullptr, lim);
+      }
+      __syncwarp();
+    }
+  } else {
+    setmaxnreg_inc<176>();
+    // ------------------------------------------------------------ softmax warpgroup
+    const int r = warp * 32 + lane;  // packed row = TMEM lane
+    const int i = min(r / p.G, p.Nq - 1);  // query (rows past M are padding)
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const uint32_t s_tm = tbase + lane_off, o_tm = tbase + lane_off + 128u;
+    const float cl2 = p.scale_log2;
+    const int lim_row = CAUSAL ? min(len_k, i + off + 1) : len_k;  // keys [0, lim_row) visible
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!__all_sync(FULL, mbar_wait(s_full, j & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Two passes over S in 64-column halves (the row maximum first, then the
+      // exponentials), so a thread holds 64 scores instead of 128: two CTAs per SM
+      // leave the softmax warpgroup about 200 registers.
+      const int jg = jb0 + j;
+      const bool masked = jg >= nfull;
+      const int nvis = lim_row - 128 * jg;  // columns [0, nvis) of this block are visible
+      float mx = -INFINITY;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(s_tm + 64u * hf, sr);
+        tmem_ld32(s_tm + 64u * hf + 32u, sr + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float v = (masked && 64 * hf + c >= nvis) ? -INFINITY : __uint_as_float(sr[c]);
+          mx = fmaxf(mx, v);
+        }
+      }
+      if (j == 0) {
+        m = mx;
+      } else if (__any_sync(FULL, (mx - m) * cl2 > 8.0f)) {
+        // lazy correction (PV(j-1) is complete: S(j) was issued after it)
+        const float m_new = fmaxf(m, mx);
+        const float alpha = (m_new == -INFINITY) ? 1.f : dec_ex2((m - m_new) * cl2);
+        m = m_new;
+        l *= alpha;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(o_tm + 32u * c, orr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) orr[u] = __float_as_uint(__uint_as_float(orr[u]) * alpha);
+          tmem_st32(o_tm + 32u * c, orr);
+        }
+        tmem_wait_st();
+      }
+      // a row with no visible key so far keeps m = -inf and gets p = 0
+      const float neg = (m == -INFINITY) ? 0.f : -m * cl2;
+      float sum = 0.f;
+      // P of half hf goes to packed columns [32 hf, 32 hf + 32), over S columns this
+      // thread has already read (half 1's scores, columns 64-127, are untouched by it)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(s_tm + 64u * hf, sr);
+        tmem_ld32(s_tm + 64u * hf + 32u, sr + 32);
+        tmem_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int c = 64 * hf + 2 * u;
+          const float s0 = (masked && c >= nvis) ? -INFINITY : __uint_as_float(sr[2 * u]);
+          const float s1 = (masked && c + 1 >= nvis) ? -INFINITY : __uint_as_float(sr[2 * u + 1]);
+          const float p0 = dec_ex2(fmaf(s0, cl2, neg));
+          const float p1 = dec_ex2(fmaf(s1, cl2, neg));
+          sum += p0 + p1;
+          pk[u] = dec_pack2<BF16>(p0, p1);
+        }
+        tmem_st32(s_tm + 32u * hf, pk);
+      }
+      l += sum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && !mbar_wait(o_done, 0, abort_flag, lim)) ok = false;
+    if (!ok) {
+      *wg_fail = 1;
+      fail();
+    }
+    named_bar_sync_n(1, 128);
+    if (*wg_fail == 0) {
+      tc_fence_after();
+      const bool has = l > 0.f;
+      const float inv = has ? 1.0f / l : 0.f;
+      const float lse = has ? m * p.scale + logf(l) : -INFINITY;
+      const bool live = r < p.M;
+      const int h = hkv * p.G + r % p.G;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(o_tm + 32u * c, orr);
+        tmem_wait_ld();
+        if (!live) continue;
+        if (p.S == 1) {
+          uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D + 32 * c;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
+            w.y = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
+            w.z = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
+            w.w = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
+            reinterpret_cast<uint4*>(orow)[u] = w;
+          }
+        } else {
+          const long long prow = (static_cast<long long>(bh) * p.S + s) * p.M + r;
+          float4* orow = reinterpret_cast<float4*>(p.opart + prow * D + 32 * c);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            orow[u] = make_float4(__uint_as_float(orr[4 * u]) * inv, __uint_as_float(orr[4 * u + 1]) * inv,
+                                  __uint_as_float(orr[4 * u + 2]) * inv, __uint_as_float(orr[4 * u + 3]) * inv);
+        }
+      }
+      if (live) {
+        if (p.S == 1)
+          p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = lse;
+        else
+          p.lpart[(static_cast<long long>(bh) * p.S + s) * p.M + r] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// Merges the splits of every packed row: lse = ln sum_s e^{lse_s},
+// O = sum_s e^{lse_s - lse} O_s (a split that saw no key has lse_s = -inf, weight 0).
+// One warp per row, lanes over the row's d/4 float4 columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_decode_combine(const __grid_constant__ DecParams p) {
+  constexpr int LANES = D / 4;
+  const long long rows = static_cast<long long>(p.B) * p.Hkv * p.M;
+  const long long warps = static_cast<long long>(gridDim.x) * 8;
+  const int lane = threadIdx.x & 31;
+  for (long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5); w < rows; w += warps) {
+    const int r = static_cast<int>(w % p.M);
+    const long long bh = w / p.M;
+    const int hkv = static_cast<int>(bh % p.Hkv), b = static_cast<int>(bh / p.Hkv);
+    const long long base = bh * p.S * p.M + r;  // partial row of split s: base + s*M
+    float mx = -INFINITY;
+    for (int s = 0; s < p.S; ++s) mx = fmaxf(mx, p.lpart[base + static_cast<long long>(s) * p.M]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float lse = -INFINITY;
+    if (mx != -INFINITY) {
+      float tot = 0.f;
+      for (int s = 0; s < p.S; ++s) tot += expf(p.lpart[base + static_cast<long long>(s) * p.M] - mx);
+      lse = mx + logf(tot);
+      for (int s = 0; s < p.S; ++s) {
+        const long long prow = base + static_cast<long long>(s) * p.M;
+        const float wgt = expf(p.lpart[prow] - lse);
+        if (lane < LANES && wgt > 0.f) {
+          const float4 v = reinterpret_cast<const float4*>(p.opart + prow * D)[lane];
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+          acc[2] += wgt * v.z;
+          acc[3] += wgt * v.w;
+        }
+      }
+    }
+    const int i = r / p.G, h = hkv * p.G + r % p.G;
+    if (lane < LANES) {
+      uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D;
+      uint2 o2;
+      o2.x = dec_pack2<BF16>(acc[0], acc[1]);
+      o2.y = dec_pack2<BF16>(acc[2], acc[3]);
+      reinterpret_cast<uint2*>(orow)[lane] = o2;
+    }
+    if (lane == 0) p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = lse;
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch_decode_t(const DecParams& p, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  auto kern = fa_decode_kernel<D, BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.B) * p.Hkv * p.S;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.S == 1) return e;
+  const long long rows = static_cast<long long>(p.B) * p.Hkv * p.M;
+  const long long blocks = (rows + 7) / 8;
+  fa_decode_combine<D, BF16><<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {
+  const bool bf = dtype == FA_BF16;
+  if (d == 128) {
+    if (bf) return causal ? launch_decode_t<128, true, true>(p, stream) : launch_decode_t<128, true, false>(p, stream);
+    return causal ? launch_decode_t<128, false, true>(p, stream) : launch_decode_t<128, false, false>(p, stream);
+  }
+  if (bf) return causal ? launch_decode_t<64, true, true>(p, stream) : launch_decode_t<64, true, false>(p, stream);
+  return causal ? launch_decode_t<64, false, true>(p, stream) : launch_decode_t<64, false, false>(p, stream);
+}
+
+}  // namespace fa

@@ -51,6 +51,9 @@ struct FwdParams {
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
                      fa_dtype dtype);
 // 3-D map over a packed [total, H, d] 16-bit tensor, box = {64, 1, rows}, 128-byte swizzle.
+// 4-D map over a [B, N, H, d] 16-bit tensor with box = {64, box_h, box_rows, 1}.
+bool encode_bshd_box_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_h, int box_rows,
+                         fa_dtype dtype);
 bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d, int box_rows, fa_dtype dtype);
 
 struct BwdParams {
@@ -72,6 +75,24 @@ struct BwdParams {
   uint64_t wait_limit_ns;
   Seqlens vl;  // varlen: packed layouts ([total, H, d] tensors, lse [Hq, total_q])
 };
+
+// Decode-shaped forward with split keys.
+struct DecParams {
+  CUtensorMap tm_q;        // 4-D over q [B, Nq, Hq, d], box {64, G, Nq, 1}: the group's rows
+  CUtensorMap tm_k, tm_v;  // 4-D over the caches [B, Nmax, Hkv, d], box {64, 1, 128, 1}
+  const int* seqlens_k;    // [B] keys in the cache of each sequence (device)
+  uint16_t* o;             // [B, Nq, Hq, d]
+  float* lse;              // [B, Hq, Nq]
+  float* opart;            // splits > 1: [B*Hkv*S, M, d] normalised partial outputs (fp32)
+  float* lpart;            // splits > 1: [B*Hkv*S, M] partial log-sum-exp
+  unsigned* err;
+  int B, Hq, Hkv, Nq, Nmax;
+  int G, M;                // G = Hq / Hkv, M = G * Nq packed rows (<= 128)
+  int S, cps;              // splits, key blocks of 128 per split
+  float scale, scale_log2;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_decode(const DecParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
 
 // Workspace layout for the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {

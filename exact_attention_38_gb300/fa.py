@@ -52,6 +52,12 @@ def _load():
     lib.fa_bwd_varlen.restype = i
     lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_fwd_decode.argtypes = [vp] * 6 + [i] * 7 + [f, i, i, vp, sz, vp]
+    lib.fa_fwd_decode.restype = i
+    lib.fa_decode_workspace_size.argtypes = [i] * 7
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode_num_splits.argtypes = [i] * 7
+    lib.fa_decode_num_splits.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_check_device_error.argtypes = [vp]
@@ -109,6 +115,21 @@ def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, used_q, used_k,
     return lib.fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, used_q, used_k, B, Hq, Hkv, total_q,
                              total_k, max_q, max_k, d, int(causal), float(scale), int(dtype), workspace,
                              int(workspace_bytes), stream)
+
+
+def fa_fwd_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, Nq, Nmax, d, causal, scale, num_splits,
+                  dtype, workspace, workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_fwd_decode``."""
+    return lib.fa_fwd_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, Nq, Nmax, d, int(causal),
+                             float(scale), int(num_splits), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_decode_workspace_size(B, Hq, Hkv, Nq, Nmax, d, num_splits=0) -> int:
+    return int(lib.fa_decode_workspace_size(B, Hq, Hkv, Nq, Nmax, d, num_splits))
+
+
+def fa_decode_num_splits(B, Hq, Hkv, Nq, Nmax, d, num_splits=0) -> int:
+    return int(lib.fa_decode_num_splits(B, Hq, Hkv, Nq, Nmax, d, num_splits))
 
 
 def fa_selftest_wait_timeout(limit_us, stream) -> int:
@@ -228,6 +249,32 @@ def backward_varlen(dout, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqle
     if st != FA_OK:
         raise FaError(st, "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def forward_decode(q, k_cache, v_cache, cache_seqlens, causal=False, scale=None, num_splits=0, out=None, lse=None,
+                   workspace=None, stream=None):
+    """Decode forward: q [B,Nq,Hq,d] against caches [B,Nmax,Hkv,d] with per-sequence
+    lengths ``cache_seqlens`` (int32 CUDA [B]).  Returns (o [B,Nq,Hq,d], lse [B,Hq,Nq])."""
+    if q.dim() != 4 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [B,Nq,Hq,d] and the caches [B,Nmax,Hkv,d]")
+    B, Nq, Hq, d = q.shape
+    Nmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape[0] != B or k_cache.shape[3] != d or q.dtype not in _DT or k_cache.dtype != q.dtype:
+        raise ValueError("q and the caches must share B, d and a 16-bit dtype")
+    if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != B or not cache_seqlens.is_cuda:
+        raise ValueError("cache_seqlens must be an int32 CUDA vector of B lengths")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = fa_decode_workspace_size(B, Hq, Hkv, Nq, Nmax, d, num_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = fa_fwd_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                       Nq, Nmax, d, causal, scale, num_splits, _DT[q.dtype], _ptr(workspace),
+                       workspace.numel() if workspace is not None else 0, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_decode")
+    return o, lse
 
 
 def check_device_error(stream=None):

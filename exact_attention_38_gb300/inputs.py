@@ -68,3 +68,16 @@ def make_varlen_inputs(seg_q, seg_k, Hq, Hkv, d, dtype="bf16", seed=0):
     cu_q[1:] = torch.cumsum(torch.tensor(list(seg_q), dtype=torch.int64), 0).to(torch.int32)
     cu_k[1:] = torch.cumsum(torch.tensor(list(seg_k), dtype=torch.int64), 0).to(torch.int32)
     return {"q": q.to(tdt), "k": k.to(tdt), "v": v.to(tdt), "do": do.to(tdt), "cu_q": cu_q, "cu_k": cu_k}
+
+
+def make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype="bf16", seed=0):
+    """Decode-shaped inputs: CPU tensors q [B, Nq, Hq, d] and caches k, v
+    [B, Nmax, Hkv, d] (every cache row drawn, including rows past a sequence's length).
+    Same recipe as ``make_inputs``: one CPU generator, fp32 normals in the order q, k, v,
+    rounded to nearest into the 16-bit type."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((B, Nq, Hq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
+    return {"q": q.to(tdt), "k": k.to(tdt), "v": v.to(tdt)}

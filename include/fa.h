@@ -124,7 +124,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *    lengths this is the usual j <= i).  A query that sees no key (len_k = 0, or
  *    i < len_q - len_k under the mask) gets o = 0, lse = -inf, and zero gradients.
  *  - Rows that belong to no sequence (the padding past seqused, gaps between
- *    segments) are not written by any call.
+ *    segments) are not written by any call.  They are read, though (a tile may run past
+ *    its sequence), and must hold finite values: masked products multiply them by 0,
+ *    and 0 * NaN is NaN.
  *  - The offsets and lengths are read by the kernels, not on the host.  A sequence
  *    whose values contradict total_* / max_seqlen_* (negative length, segment past the
  *    end, length above the maximum, decreasing offsets) is skipped, and the next
@@ -161,6 +163,47 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         const int* cu_seqlens_k, const int* seqused_q, const int* seqused_k, int B, int Hq, int Hkv,
                         int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale,
                         fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Decode: a few new queries per sequence against a key/value cache
+ * ----------------------------------------------------------------
+ * The pages separate decode from prefill ("FlashAttention-2: atención eficiente en GPU
+ * para contextos largos", section "Cómo documentar una diferencia técnica") and split
+ * work along the sequence when batch and heads leave the GPU idle (section "Tres
+ * mejoras en la utilización de la GPU").  The interface is a reading:
+ *   q          : [B, Nq, Hq, d]     the new queries (dtype)
+ *   k_cache,
+ *   v_cache    : [B, Nmax, Hkv, d]  caches (dtype); sequence b uses rows [0, len_b)
+ *   cache_seqlens : DEVICE int32 [B], len_b in [0, Nmax] (the new tokens' keys are
+ *                   already in the cache: they are its last Nq rows)
+ *   o          : [B, Nq, Hq, d] output (dtype);  lse : [B, Hq, Nq] fp32
+ * Causal: query i sees key j iff j <= i + len_b - Nq (bottom-right alignment, as for
+ * the variable-length calls); a query that sees no key gets o = 0, lse = -inf.
+ * The key range of each (batch, key/value head) is split into num_splits parts
+ * processed in parallel and merged by their log-sum-exp (num_splits = 0 picks a count
+ * from the sizes).  Requires d in {64, 128} and (Hq / Hkv) * Nq <= 128 (the group's
+ * queries share one 128-row tile).  Cache rows at or past len_b must hold finite
+ * values (they are read and masked, and 0 * NaN would still be NaN); a zero-filled
+ * cache satisfies this.  A len_b outside [0, Nmax] is reported as FA_ERR_INVALID by
+ * the next fa_check_device_error(), and that sequence is not written.
+ */
+
+/* Split count fa_fwd_decode will use for these sizes (0 for invalid sizes). */
+int fa_decode_num_splits(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits);
+
+/*
+ * Workspace bytes for fa_fwd_decode: 0 with one split, else fp32 partial outputs
+ * [B*Hkv*S, (Hq/Hkv)*Nq, d] and partial log-sum-exps [B*Hkv*S, (Hq/Hkv)*Nq], each
+ * rounded up to 256 bytes.  0 also for invalid sizes.
+ */
+size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits);
+
+/* Decode forward (see above).  workspace: 256-byte aligned, at least
+ * fa_decode_workspace_size() bytes (may be NULL when that is 0). */
+fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache, const int* cache_seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Nq, int Nmax, int d, int causal, float scale,
+                        int num_splits, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                        fa_stream_t stream);
 
 /*
  * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).

@@ -165,3 +165,51 @@ def test_varlen_workspace_size(lib):
     assert lib.fa_bwd_varlen_workspace_size(3, 4, 200, 128) == lib.fa_bwd_workspace_size(3, 4, 4, 200, 128)
     assert lib.fa_bwd_varlen_workspace_size(3, 4, 0, 128) == lib.fa_bwd_workspace_size(3, 4, 4, 64, 128)
     assert lib.fa_bwd_varlen_workspace_size(3, 4, 10, 96) == 0
+
+
+def _decode(lib, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, cl=0x40000, o=0x50000, lse=0x60000, B=2, Hq=8, Hkv=2, Nq=1,
+             Nmax=4096, d=128, causal=1, scale=0.088, splits=0, dtype=0, ws=0x100000, ws_bytes=None)
+    a.update(kw)
+    i = ctypes.c_int
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.fa_decode_workspace_size.argtypes = [i] * 7
+    need = lib.fa_decode_workspace_size(a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nmax"], a["d"], a["splits"])
+    ws_bytes = need if a["ws_bytes"] is None else a["ws_bytes"]
+    vp = ctypes.c_void_p
+    f = lib.fa_fwd_decode
+    f.argtypes = [vp] * 6 + [i] * 7 + [ctypes.c_float, i, i, vp, ctypes.c_size_t, vp]
+    f.restype = i
+    return f(a["q"], a["k"], a["v"], a["cl"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nmax"],
+             a["d"], a["causal"], a["scale"], a["splits"], a["dtype"], a["ws"], ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(v=0x30008), 1), (dict(cl=None), 1), (dict(cl=0x40002), 1), (dict(Nq=0), 1),
+    (dict(Nmax=0), 1), (dict(Hq=6, Hkv=4), 1), (dict(splits=-1), 1), (dict(scale=-1.0), 1), (dict(d=256), 2),
+    (dict(Hq=32, Hkv=1, Nq=8), 2),  # 256 packed rows > one 128-row tile
+    (dict(ws=None), 1), (dict(ws_bytes=16), 1),
+])
+def test_decode_argument_errors_need_no_device(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_decode_split_count_and_workspace(lib):
+    i = ctypes.c_int
+    lib.fa_decode_num_splits.restype = i
+    lib.fa_decode_num_splits.argtypes = [i] * 7
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.fa_decode_workspace_size.argtypes = [i] * 7
+    # forced counts are capped by the number of 128-key blocks, then trimmed so no
+    # split is empty (9 blocks in 4 splits of 3 -> 3 splits)
+    assert lib.fa_decode_num_splits(1, 8, 2, 1, 1152, 128, 4) == 3
+    assert lib.fa_decode_num_splits(1, 8, 2, 1, 200, 128, 50) == 2
+    assert lib.fa_decode_num_splits(1, 8, 2, 1, 200, 128, 1) == 1
+    # automatic: more splits when batch x kv-heads is small
+    assert lib.fa_decode_num_splits(1, 32, 8, 1, 65536, 128, 0) > lib.fa_decode_num_splits(64, 32, 8, 1, 65536, 128, 0)
+    # one split needs no workspace; otherwise partial outputs + partial lse
+    assert lib.fa_decode_workspace_size(1, 8, 2, 1, 4096, 128, 1) == 0
+    S = lib.fa_decode_num_splits(1, 8, 2, 2, 4096, 128, 5)
+    rows = 1 * 2 * S * 4 * 2
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert lib.fa_decode_workspace_size(1, 8, 2, 2, 4096, 128, 5) == up(rows * 128 * 4) + up(rows * 4)

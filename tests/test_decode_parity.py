@@ -1,0 +1,75 @@
+"""Decode forward (a few new queries against a key/value cache, keys split across CTAs
+and merged by log-sum-exp): the CUDA path against the fp64 oracle.
+
+Each sequence b is checked as one unequal-length problem of the oracle
+(``oracle.attn_fwd_qk`` with Nq queries and the first len_b cache rows, mask aligned at
+the bottom-right corner).  Covers one and several new queries, GQA group packing, split
+counts 1 / automatic / forced, sequences shorter than Nq (rows that see no key), an empty
+cache, both 16-bit types and head dimensions, and a length out of range."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import ATOL, LSE_ATOL, assert_close, f64
+from exact_attention_38_gb300.inputs import make_decode_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(fa, B, Nq, Nmax, Hq, Hkv, d, lens, dtype, causal, num_splits, seed):
+    x = make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype=dtype, seed=seed)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward_decode(q, k, v, cl, causal=causal, scale=scale, num_splits=num_splits)
+    fa.check_device_error()
+    o, lse = f64(o.cpu()), lse.cpu().numpy().astype(np.float64)
+    xo = {n: f64(x[n]) for n in ("q", "k", "v")}
+    for b in range(B):
+        ro, rl = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], causal, scale)
+        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype])
+        assert np.array_equal(np.isneginf(lse[b]), np.isneginf(rl)), f"lse[b={b}]: rows without keys must be -inf"
+        fin = np.isfinite(rl)
+        if fin.any():
+            assert np.max(np.abs(lse[b][fin] - rl[fin])) <= LSE_ATOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("num_splits", [0, 1, 7])
+def test_single_query_gqa(fa_lib, causal, num_splits):
+    _check(fa_lib, 3, 1, 3000, 8, 2, 128, [1, 2999, 777], "bf16", causal, num_splits, 41)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_several_queries_short_caches(fa_lib, causal):
+    # Nq = 4 new tokens; the second sequence is shorter than Nq (its first queries see
+    # nothing under the mask), the third is empty
+    _check(fa_lib, 3, 4, 1000, 16, 2, 128, [1000, 3, 0], "bf16", causal, 0, 42)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_full_tile_fp16_d64(fa_lib, causal, num_splits):
+    # G * Nq = 8 * 16 = 128 packed rows: the whole tile
+    _check(fa_lib, 2, 16, 2100, 16, 2, 64, [2100, 1234], "fp16", causal, num_splits, 43)
+
+
+def test_long_cache_many_splits(fa_lib):
+    _check(fa_lib, 1, 2, 40000, 32, 8, 128, [39999], "bf16", True, 0, 44)
+
+
+def test_length_out_of_range_is_reported(fa_lib):
+    fa = fa_lib
+    x = make_decode_inputs(2, 1, 256, 4, 4, 64, dtype="bf16", seed=45)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    cl = torch.tensor([100, 300], dtype=torch.int32, device="cuda")  # 300 > Nmax
+    o = torch.full_like(q, float("nan"))
+    fa.forward_decode(q, k, v, cl, out=o, num_splits=1)
+    with pytest.raises(fa.FaError) as e:
+        fa.check_device_error()
+    assert e.value.status == fa.FA_ERR_INVALID
+    assert torch.isnan(o[1]).all() and not torch.isnan(o[0]).any()
