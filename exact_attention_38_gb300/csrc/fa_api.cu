@@ -76,16 +76,17 @@ fa_status check_varlen(int B, int Hq, int Hkv, int total_q, int total_k, int max
 
 bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// Split count of the decode pass: enough CTAs for about four per SM slot on a 152-SM
-// part at two CTAs per SM (a fixed target, so the workspace size does not depend on the
-// device), never more splits than key blocks; `want` > 0 overrides the target.
+// Split count of the decode pass: as many splits as fit one wave of CTA slots on a
+// 152-SM part at two CTAs per SM (304; a fixed target, so the workspace size does not
+// depend on the device; measured best on GB300 against 2-4x more CTAs), never more
+// splits than key blocks; `want` > 0 overrides the target.
 struct DecodeSplit {
   int S, cps;
 };
 DecodeSplit decode_split(int B, int Hkv, int Nmax, int want) {
   const int nkb = (Nmax + 127) / 128;
   const long long units = static_cast<long long>(B) * Hkv;
-  long long S = want > 0 ? want : (1216 + units - 1) / units;
+  long long S = want > 0 ? want : 304 / units;
   if (S > nkb) S = nkb;
   if (S < 1) S = 1;
   const int cps = static_cast<int>((nkb + S - 1) / S);

@@ -278,9 +278,16 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
+      if (warp * 32 >= p.M) {
+        // every row of this warp is padding: keep the barrier protocol, skip the work
+        // (its P stays whatever S left there; padding rows' outputs are never stored)
+        tc_fence_before();
+        mbar_arrive(p_full);
+        continue;
+      }
       // Two passes over S in 64-column halves (the row maximum first, then the
-      // exponentials), so a thread holds 64 scores instead of 128: two CTAs per SM
-      // leave the softmax warpgroup about 200 registers.
+      // exponentials), so a thread holds 64 scores instead of 128 and the softmax
+      // warpgroup fits the 176 registers two CTAs per SM leave it.
       const int jg = jb0 + j;
       const bool masked = jg >= nfull;
       const int nvis = lim_row - 128 * jg;  // columns [0, nvis) of this block are visible
