@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward through fa_bwd_deterministic (fixed summation order)")
     ap.add_argument("--pass", dest="which", default="step", choices=["step", "fwd", "bwd"])
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--B", type=int, default=None)
@@ -63,7 +65,8 @@ def parse():
 def workload(a):
     B = a.B if a.B is not None else max(1, 16384 // a.N)
     Hkv = a.Hkv if a.Hkv is not None else a.H
-    return dict(B=B, Hq=a.H, Hkv=Hkv, N=a.N, d=a.d, causal=bool(a.causal), dtype="bf16")
+    return dict(B=B, Hq=a.H, Hkv=Hkv, N=a.N, d=a.d, causal=bool(a.causal), dtype="bf16",
+                deterministic=bool(getattr(a, "deterministic", False)))
 
 
 def flops(w, which):
@@ -76,7 +79,8 @@ def flops(w, which):
 def workload_name(w, which):
     passes = {"step": "fwd+bwd", "fwd": "fwd", "bwd": "bwd"}[which]
     return (f"exact attention {passes}, B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} N={w['N']} d={w['d']} "
-            f"{w['dtype']} {'causal' if w['causal'] else 'non-causal'} ({w['B'] * w['N'] // 1024}k tokens/batch)")
+            f"{w['dtype']} {'causal' if w['causal'] else 'non-causal'} ({w['B'] * w['N'] // 1024}k tokens/batch)"
+            + (", deterministic backward" if w.get("deterministic") else ""))
 
 
 def kernel_source_digest(kernel):
@@ -269,17 +273,19 @@ def run_native(a):
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
 
+    bwd_fn = fa.fa_bwd_deterministic if a.deterministic else fa.fa_bwd
+
     def bwd():
-        st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, scale, DT,
-                       ws.data_ptr(), ws_bytes, sp)
+        st = bwd_fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, scale, DT,
+                    ws.data_ptr(), ws_bytes, sp)
         if st != fa.FA_OK:
-            raise fa.FaError(st, "fa_bwd")
+            raise fa.FaError(st, bwd_fn.__name__)
 
     parts = {"step": [("fwd", fwd), ("bwd", bwd)], "fwd": [("fwd", fwd)], "bwd": [("bwd", bwd)]}[a.which]
     if a.which == "bwd":
         fwd()
-    launches_per_step = sum({"fwd": 1, "bwd": 3}[n] for n, _ in parts)
+    launches_per_step = sum({"fwd": 1, "bwd": 3}[n] for n, _ in parts)  # deterministic: preprocess, dK/dV, dQ
 
     for _ in range(a.warmup):
         for _, fn in parts:

@@ -294,9 +294,13 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
   return bwd_workspace_layout(B, Hq, N, d).total;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
-                 fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+fa_status bwd_fixed(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                    fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream,
+                    bool deterministic) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID;
@@ -318,10 +322,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq = static_cast<uint16_t*>(dq);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
-  p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
+  p.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(w + ws.dq_acc_off);
   p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
-  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d)) return FA_ERR_CUDA;
+  if (!deterministic && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d)) return FA_ERR_CUDA;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -330,9 +334,29 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
-  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, false, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_bwd(p, d, dtype, causal != 0, false, deterministic, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_fixed(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, false);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                               int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream) {
+  return bwd_fixed(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, true);
+}
+
 
 static int varlen_npad(int max_q) { return max_q > 0 ? (max_q + 63) / 64 * 64 : 64; }
 
@@ -391,7 +415,7 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
   p.vl = Seqlens{cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, total_q, total_k, max_seqlen_q, max_seqlen_k};
-  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, true, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_bwd(p, d, dtype, causal != 0, true, false, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
     p.dvec[bh * p.Npad + n] = 0.f;
     p.l2vec[bh * p.Npad + n] = -INFINITY;
   }
-  // dQ accumulator = 0 (16 B per thread per step)
-  const long long nacc4 = static_cast<long long>(p.B) * p.Hq * D * p.Npad / 4;
+  // dQ accumulator = 0 (16 B per thread per step); none when dQ is computed elsewhere
+  const long long nacc4 = p.dq_acc ? static_cast<long long>(p.B) * p.Hq * D * p.Npad / 4 : 0;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (long long i = tid; i < nacc4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
 }
 
 // ------------------------------------------------------------------- main kernel
-template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
 __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_bwd[];
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             break;
           }
           // S^T(it) overwrites the buffer that held dQ^T(it-2): it must have been read out
-          if (it >= 2 && !__all_sync(FULL, mbar_wait(dq_free, (it - 2) & 1, abort_flag, lim))) {
+          if (DQ && it >= 2 && !__all_sync(FULL, mbar_wait(dq_free, (it - 2) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
@@ -512,11 +512,13 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             // dQ^T = K^T dS^T into the step's S^T buffer, after dV and dK above have read
             // P^T and dS^T from it (tcgen05.mma executes in issue order).  K^T: MN-major
             // view of the K tile, d padded to 128 rows; dS^T: MN-major, queries contiguous.
+            if (DQ) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tbase + C::T_S + 64u * bb, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq,
-                     kk > 0);
-            mma_commit(dq_full(bb));
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tbase + C::T_S + 64u * bb, dK_mn + u16(kk * 2048), dDS_mn + dss + u16(kk * 2048), id_dq,
+                       kk > 0);
+              mma_commit(dq_full(bb));
+            }
             mma_commit(ds_free(bb));
           }
         }
@@ -641,7 +643,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
           dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
           dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
         }
-        *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
+        if (DQ)  // the shared-memory copy of dS^T feeds only the dQ^T product
+          *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
       }
       // P^T (16 packed columns) then dS^T (16) go back into the 32 columns of S^T this
       // warpgroup read, so neither warpgroup writes columns the other still reads
@@ -693,7 +696,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     // as [d rows x 128 B] with the 128-byte swizzle and added into the accumulator
     // ([B*Hq, d, Npad] fp32, queries contiguous) by one TMA bulk tensor reduction.
     bool ok = true;
-    for (int it = 0; it < T; ++it) {
+    for (int it = 0; it < (DQ ? T : 0); ++it) {  // without the dQ path only the dV epilogue
       const int hq = hkv * G + it / nq;
       const int q0 = 64 * (qb0 + it % nq);
       // The named barriers below span the four warps of this warpgroup, but a wait's
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   }
 }
 
-template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   int dev = 0, sms = 148;
@@ -801,7 +804,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN>;
+    auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const long long nk = VARLEN ? p.vl.max_k : p.N;
@@ -812,6 +815,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
       if (e != cudaSuccess) return e;
     }
   }
+  if (!DQ) return launch_bwd_dq(p, D, BF16 ? FA_BF16 : FA_FP16, CAUSAL, stream);
   {
     const long long grid = static_cast<long long>(p.B) * p.Hq * (VARLEN ? p.Npad / 64 : (p.N + 63) / 64);
     fa_bwd_dq_convert<D, BF16, VARLEN><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
@@ -820,15 +824,24 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
 }
 
 template <int D, bool BF16>
-static cudaError_t launch_bwd_d(const BwdParams& p, bool causal, bool varlen, cudaStream_t stream) {
-  if (varlen) return causal ? launch_bwd_t<D, BF16, true, true>(p, stream) : launch_bwd_t<D, BF16, false, true>(p, stream);
-  return causal ? launch_bwd_t<D, BF16, true, false>(p, stream) : launch_bwd_t<D, BF16, false, false>(p, stream);
+static cudaError_t launch_bwd_d(const BwdParams& p, bool causal, bool varlen, bool deterministic,
+                                cudaStream_t stream) {
+  if (varlen)
+    return causal ? launch_bwd_t<D, BF16, true, true, true>(p, stream) : launch_bwd_t<D, BF16, false, true, true>(p, stream);
+  if (deterministic)
+    return causal ? launch_bwd_t<D, BF16, true, false, false>(p, stream)
+                  : launch_bwd_t<D, BF16, false, false, false>(p, stream);
+  return causal ? launch_bwd_t<D, BF16, true, false, true>(p, stream) : launch_bwd_t<D, BF16, false, false, true>(p, stream);
 }
 
-cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, bool deterministic,
+                       cudaStream_t stream) {
   const bool bf = dtype == FA_BF16;
-  if (d == 128) return bf ? launch_bwd_d<128, true>(p, causal, varlen, stream) : launch_bwd_d<128, false>(p, causal, varlen, stream);
-  return bf ? launch_bwd_d<64, true>(p, causal, varlen, stream) : launch_bwd_d<64, false>(p, causal, varlen, stream);
+  if (d == 128)
+    return bf ? launch_bwd_d<128, true>(p, causal, varlen, deterministic, stream)
+              : launch_bwd_d<128, false>(p, causal, varlen, deterministic, stream);
+  return bf ? launch_bwd_d<64, true>(p, causal, varlen, deterministic, stream)
+            : launch_bwd_d<64, false>(p, causal, varlen, deterministic, stream);
 }
 
 }  // namespace fa

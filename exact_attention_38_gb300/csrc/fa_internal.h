@@ -106,7 +106,11 @@ bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, in
 unsigned* device_error_word();  // address of this device's error word (device memory)
 
 cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
+// deterministic: dK/dV from the key-block kernel without its dQ path, then dQ from the
+// query-tile kernel (fa_bwd_dq.cu) in a fixed summation order; p.dq_acc must be null.
+cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, bool deterministic,
+                       cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
 
 // Geometry of sequence b of a variable-length launch; false if its offsets or length
 // contradict the launch's sizes.

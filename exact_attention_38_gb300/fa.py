@@ -42,6 +42,8 @@ def _load():
     lib.fa_fwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd_deterministic.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
@@ -86,6 +88,13 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, d
     """Mirror of the C ``fa_bwd``."""
     return lib.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
                       int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, workspace,
+                         workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_bwd_deterministic``."""
+    return lib.fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
+                                    int(dtype), workspace, int(workspace_bytes), stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, stream) -> int:
@@ -181,8 +190,9 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
 
 
 def backward(dout, q, k, v, o, lse, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
-             stream=None):
-    """Returns (dq, dk, dv); allocates the workspace with torch if not given."""
+             stream=None, deterministic=False):
+    """Returns (dq, dk, dv); allocates the workspace with torch if not given.  With
+    ``deterministic`` the results are identical bit for bit from run to run."""
     B, N, Hq, Hkv, d = _shapes(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d)
@@ -191,10 +201,11 @@ def backward(dout, q, k, v, o, lse, causal=False, scale=None, workspace=None, dq
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
-                Hkv, N, d, causal, scale, _DT[q.dtype], _ptr(workspace), workspace.numel(), _stream(stream))
+    fn = fa_bwd_deterministic if deterministic else fa_bwd
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+            Hkv, N, d, causal, scale, _DT[q.dtype], _ptr(workspace), workspace.numel(), _stream(stream))
     if st != FA_OK:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, fn.__name__)
     return dq, dk, dv
 
 

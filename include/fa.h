@@ -206,6 +206,22 @@ fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
                         fa_stream_t stream);
 
 /*
+ * fa_bwd with a fixed summation order: the same arguments, results within the same
+ * tolerance, and dq, dk, dv identical bit for bit from run to run (fa_bwd's dq depends
+ * on the order in which key blocks land their fp32 additions).  The dK/dV kernel runs
+ * without its dQ path, and a second kernel over 128-query tiles recomputes S and dP and
+ * accumulates dQ = scale * sum_j dS_j K_j over the key blocks in ascending order in
+ * tensor memory: seven GEMM-shaped products per (query, key) block instead of five.
+ * The pages mention no deterministic mode; this is the plain way to get one without
+ * atomics or cross-block waits.  workspace as for fa_bwd (only its D and lse parts are
+ * used).
+ */
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                               int causal, float scale, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream);
+
+/*
  * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
