@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="decode forward: --B sequences (default 8) of --N cached keys (default 16384), "
                          "--Nq new queries, Hq=--H (default 32 here), Hkv=--Hkv (default 8 here)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="forward only with E4M3 q, k, v (per-tensor descales), bf16 output")
     ap.add_argument("--Nq", type=int, default=1)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--min-len", type=int, default=512)
@@ -571,10 +573,69 @@ def run_decode(a):
     print(json.dumps(line), flush=True)
 
 
+def run_fp8(a):
+    import torch
+
+    from exact_attention_38_gb300 import fa
+    from exact_attention_38_gb300.inputs import make_fp8_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = workload(a)
+    B, Hq, Hkv, N, d, causal = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], w["causal"]
+    x = make_fp8_inputs(B, N, Hq, Hkv, d, seed=3)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_fwd_fp8_workspace_size(B, Hkv, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    scale = 1.0 / math.sqrt(d)
+
+    def fwd():
+        st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, d,
+                           causal, scale, x["q_descale"], x["k_descale"], x["v_descale"], ws.data_ptr(), ws_bytes, sp)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_fp8")
+
+    for _ in range(a.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        for i in range(a.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    fa.check_device_error()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    tf = flops(w, "fwd") / (ms * 1e-3) / 1e12
+    peak_bf16, _, peak_kind = measured_peaks()
+    peak = 2.0 * peak_bf16  # E4M3 dense rate = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    line = {"metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": workload_name(w, "fwd").replace("bf16", "e4m3 in, bf16 out"),
+                       "l2": "flushed between steps (outside the timed events)"},
+            "roofline": {"bound": "tensor", "kernel": "fa_fwd_fp8_kernel (+ V transpose)", "achieved": tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 burst x 2 (E4M3 / bf16 nominal ratio)"},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": 2 * a.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.fp8:
+        run_fp8(a)
     elif a.decode:
         run_decode(a)
     elif a.varlen:

@@ -189,6 +189,32 @@ bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d,
   return r == CUDA_SUCCESS;
 }
 
+bool encode_bshd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d,
+                                 static_cast<cuuint64_t>(N) * H * d};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_vt_u8_map(CUtensorMap* map, const void* base, int BH, int d, int Npad) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Npad), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Npad), static_cast<cuuint64_t>(d) * Npad};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(d), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, int d) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) return false;
@@ -470,6 +496,47 @@ fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
   const cudaError_t e = launch_decode(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d) {
+  if (check_sizes(B, Hkv, Hkv, N, d, 1.0f, FA_BF16) != FA_OK || d != 128) return 0;
+  const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+  return (static_cast<size_t>(B) * Hkv * d * npad + 255) & ~size_t(255);
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                     int d, int causal, float scale, float q_descale, float k_descale, float v_descale,
+                     void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+  const fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, FA_BF16);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  for (float f : {q_descale, k_descale, v_descale})
+    if (!(f > 0.f) || !std::isfinite(f)) return FA_ERR_INVALID;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < fa_fwd_fp8_workspace_size(B, Hkv, N, d))
+    return FA_ERR_INVALID;
+  Fp8Params p{};
+  p.Npad = (N + 127) / 128 * 128;
+  if (!encode_bshd_u8_map(&p.tm_q, q, B, N, Hq, d, 128) || !encode_bshd_u8_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
+      !encode_vt_u8_map(&p.tm_vt, workspace, B * Hkv, d, p.Npad))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  p.v = static_cast<const uint8_t*>(v);
+  p.vt = static_cast<uint8_t*>(workspace);
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.score_scale = scale * q_descale * k_descale;
+  p.score_log2 = p.score_scale * 1.4426950408889634f;
+  p.out_scale = v_descale / 256.0f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_fwd_fp8(p, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -94,6 +94,27 @@ struct DecParams {
 };
 cudaError_t launch_decode(const DecParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
 
+// FP8 (E4M3) forward, head dimension 128.
+struct Fp8Params {
+  CUtensorMap tm_q, tm_k;  // 4-D over E4M3 [B, N, H, 128], box {128, 1, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_vt;       // 3-D over V^T [B*Hkv, 128, Npad] (keys contiguous), box {128, 128, 1}
+  const uint8_t* v;        // [B, N, Hkv, 128] E4M3 (input of the transpose)
+  uint8_t* vt;             // workspace: V^T, zero past N
+  uint16_t* o;             // [B, N, Hq, 128] bf16
+  float* lse;              // [B, Hq, N]
+  unsigned* err;
+  int B, Hq, Hkv, N, Npad;  // Npad = N rounded up to 128
+  float score_log2;         // scale * q_descale * k_descale * log2(e)
+  float score_scale;        // scale * q_descale * k_descale
+  float out_scale;          // v_descale / 2^8 (P is rounded to E4M3 as P * 2^8)
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream);
+// 4-D map over an 8-bit [B, N, H, d] tensor, box {d, 1, rows, 1} (d = 128 bytes).
+bool encode_bshd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows);
+// 3-D map over an 8-bit [BH, d, Npad] tensor, box {128, d, 1}.
+bool encode_vt_u8_map(CUtensorMap* map, const void* base, int BH, int d, int Npad);
+
 // Workspace layout for the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
   size_t dq_acc_off, dvec_off, l2vec_off, total;

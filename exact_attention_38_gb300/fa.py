@@ -60,6 +60,10 @@ def _load():
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode_num_splits.argtypes = [i] * 7
     lib.fa_decode_num_splits.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp] * 5 + [i] * 6 + [f, f, f, f, vp, sz, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i] * 4
+    lib.fa_fwd_fp8_workspace_size.restype = sz
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_check_device_error.argtypes = [vp]
@@ -139,6 +143,17 @@ def fa_decode_workspace_size(B, Hq, Hkv, Nq, Nmax, d, num_splits=0) -> int:
 
 def fa_decode_num_splits(B, Hq, Hkv, Nq, Nmax, d, num_splits=0) -> int:
     return int(lib.fa_decode_num_splits(B, Hq, Hkv, Nq, Nmax, d, num_splits))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, q_descale, k_descale, v_descale, workspace,
+               workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_fwd_fp8``."""
+    return lib.fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, N, d, int(causal), float(scale), float(q_descale),
+                          float(k_descale), float(v_descale), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_fp8_workspace_size(B, Hkv, N, d) -> int:
+    return int(lib.fa_fwd_fp8_workspace_size(B, Hkv, N, d))
 
 
 def fa_selftest_wait_timeout(limit_us, stream) -> int:
@@ -285,6 +300,30 @@ def forward_decode(q, k_cache, v_cache, cache_seqlens, causal=False, scale=None,
                        workspace.numel() if workspace is not None else 0, _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_decode")
+    return o, lse
+
+
+def forward_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=None, out=None, lse=None,
+                workspace=None, stream=None):
+    """FP8 forward: q [B,N,Hq,128], k/v [B,N,Hkv,128] as torch.float8_e4m3fn (or uint8
+    holding E4M3 bytes) with per-tensor descales.  Returns (o bf16, lse fp32)."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,N,Hq,d], k and v [B,N,Hkv,d]")
+    for t in (q, k, v):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous 8-bit CUDA tensors")
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = fa_fwd_fp8_workspace_size(B, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, causal, scale, q_descale,
+                    k_descale, v_descale, _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
     return o, lse
 
 

@@ -81,3 +81,19 @@ def make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype="bf16", seed=0):
     k = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
     v = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
     return {"q": q.to(tdt), "k": k.to(tdt), "v": v.to(tdt)}
+
+
+def make_fp8_inputs(B, N, Hq, Hkv, d, seed=0):
+    """E4M3 inputs with one descale per tensor: the ``make_inputs`` draw (q, k, v fp32
+    normals from one CPU generator), each tensor divided by its descale = amax / 448 and
+    rounded to nearest E4M3 (torch.float8_e4m3fn).  Returns a dict with CPU tensors q, k,
+    v (E4M3) and floats q_descale, k_descale, v_descale; real value = E4M3 value x
+    descale."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    out = {}
+    for name, shape in (("q", (B, N, Hq, d)), ("k", (B, N, Hkv, d)), ("v", (B, N, Hkv, d))):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        ds = float(x.abs().max()) / 448.0
+        out[name] = (x / ds).to(torch.float8_e4m3fn)
+        out[name + "_descale"] = ds
+    return out

@@ -222,6 +222,28 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                fa_stream_t stream);
 
 /*
+ * FP8 (E4M3) forward
+ * ------------------
+ * The pages report an 8-bit forward ("FlashAttention-T: Optimización GPU para LLMs
+ * Escalables", section "Innovaciones técnicas frente a FlashAttention original"); the
+ * interface and scaling are a reading:
+ *   q [B,N,Hq,128], k/v [B,N,Hkv,128]: E4M3 bytes (the OCP FP8 format with 4 exponent
+ *   and 3 mantissa bits, NaN only at 0x7F/0xFF), real value = stored value x the
+ *   tensor's descale (q_descale, k_descale, v_descale: finite, > 0).
+ *   o [B,N,Hq,128]: bf16.  lse [B,Hq,N]: fp32, natural log of the scaled scores.
+ * Scores and their softmax are computed in fp32 from the 8-bit products; P is rounded to
+ * E4M3 (as P * 2^8) for the P V product, so O carries up to 2^-4 relative error per term
+ * of its sum over keys.  Head dimension 128 only (FA_ERR_UNSUPPORTED otherwise).
+ * workspace: at least fa_fwd_fp8_workspace_size() bytes, 256-byte aligned; it receives a
+ * transposed copy of V (the 8-bit P V product reads V with keys contiguous).
+ * Other conventions as fa_fwd.
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                     int d, int causal, float scale, float q_descale, float k_descale, float v_descale,
+                     void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -213,3 +213,21 @@ def test_decode_split_count_and_workspace(lib):
     rows = 1 * 2 * S * 4 * 2
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert lib.fa_decode_workspace_size(1, 8, 2, 2, 4096, 128, 5) == up(rows * 128 * 4) + up(rows * 4)
+
+
+def test_fp8_argument_errors_need_no_device(lib):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i] * 4
+    assert lib.fa_fwd_fp8_workspace_size(2, 4, 300, 128) == 2 * 4 * 128 * 384
+    assert lib.fa_fwd_fp8_workspace_size(2, 4, 300, 64) == 0
+    fn = lib.fa_fwd_fp8
+    fn.argtypes = [vp] * 5 + [i] * 6 + [f, f, f, f, vp, ctypes.c_size_t, vp]
+    fn.restype = i
+    base = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 2, 4, 4, 300, 128, 1, 0.088, 0.01, 0.01, 0.01, 0x100000,
+            2 * 4 * 128 * 384, None]
+    for idx, val, code in [(0, None, 1), (1, 0x20008, 1), (9, 64, 2), (12, 0.0, 1), (14, float("nan"), 1),
+                           (15, None, 1), (16, 1024, 1), (6, 3, 1)]:
+        a = list(base)
+        a[idx] = val
+        assert fn(*a) == code, (idx, val)
