@@ -333,9 +333,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int c = 0; c < 128; ++c)
           if (c >= nvis) s[c] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float mx = rowmax128(s);
       if (j == 0) {
         m = mx;
       } else if (__any_sync(0xffffffffu, (mx - m) * cl2 > 8.0f)) {
@@ -360,13 +358,25 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       // a row with no visible key so far (only possible with variable lengths and the
       // mask) has m = -inf: its p are exp2(-inf) = 0
       const float neg = (VARLEN && CAUSAL && m == -INFINITY) ? 0.f : -m * cl2;
-      float sum = 0.f;
+      // exponent arguments two at a time (f32x2 FMA), sums in two packed accumulators
+      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg);
+      uint64_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = ex2f(fmaf(s[c], cl2, neg));
-        sum += s[c];
+      for (int c = 0; c < 128; c += 4) {
+        float a0, a1, a2, a3;
+        f2unpack(ffma2(f2pack(s[c], s[c + 1]), cl2x2, negx2), a0, a1);
+        f2unpack(ffma2(f2pack(s[c + 2], s[c + 3]), cl2x2, negx2), a2, a3);
+        s[c] = ex2f(a0);
+        s[c + 1] = ex2f(a1);
+        s[c + 2] = ex2f(a2);
+        s[c + 3] = ex2f(a3);
+        acc0 = fadd2(acc0, f2pack(s[c], s[c + 1]));
+        acc1 = fadd2(acc1, f2pack(s[c + 2], s[c + 3]));
       }
-      l += sum;
+      float sa, sb, sc2, sd;
+      f2unpack(acc0, sa, sb);
+      f2unpack(acc1, sc2, sd);
+      l += (sa + sb) + (sc2 + sd);
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) pk[i] = pack2<BF16>(s[2 * i], s[2 * i + 1]);

@@ -310,9 +310,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         for (int c = 0; c < 128; ++c)
           if (c >= nvis) s[c] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float mx = rowmax128(s);
       if (j == 0) {
         m = mx;
       } else if (__any_sync(FULL, (mx - m) * cl2 > kTau)) {
@@ -332,19 +330,26 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         tmem_wait_st();
       }
       const float neg = -m * cl2;
-      float sum = 0.f;
+      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg), ps2 = f2pack(kPScale, kPScale);
+      uint64_t acc0 = 0ull, acc1 = 0ull;
       uint32_t pk[32];
 #pragma unroll
       for (int c4 = 0; c4 < 32; ++c4) {
-        float q4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          q4[u] = f8_ex2(fmaf(s[4 * c4 + u], cl2, neg));
-          sum += q4[u];
-        }
-        pk[c4] = pack4_e4m3(q4[0] * kPScale, q4[1] * kPScale, q4[2] * kPScale, q4[3] * kPScale);
+        float a0, a1, a2, a3;
+        f2unpack(ffma2(f2pack(s[4 * c4], s[4 * c4 + 1]), cl2x2, negx2), a0, a1);
+        f2unpack(ffma2(f2pack(s[4 * c4 + 2], s[4 * c4 + 3]), cl2x2, negx2), a2, a3);
+        const uint64_t p01 = f2pack(f8_ex2(a0), f8_ex2(a1)), p23 = f2pack(f8_ex2(a2), f8_ex2(a3));
+        acc0 = fadd2(acc0, p01);
+        acc1 = fadd2(acc1, p23);
+        float q0, q1, q2, q3;
+        f2unpack(fmul2(p01, ps2), q0, q1);
+        f2unpack(fmul2(p23, ps2), q2, q3);
+        pk[c4] = pack4_e4m3(q0, q1, q2, q3);
       }
-      l += sum;
+      float sa, sb, sc2, sd;
+      f2unpack(acc0, sa, sb);
+      f2unpack(acc1, sc2, sd);
+      l += (sa + sb) + (sc2 + sd);
       tmem_st32(s_tm, pk);
       tmem_wait_st();
       tc_fence_before();

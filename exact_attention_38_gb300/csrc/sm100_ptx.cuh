@@ -66,6 +66,29 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// max(a, b, c) in one instruction (three-input form, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 128 values: four independent chains of three-input maxima.
+__device__ __forceinline__ float rowmax128(const float* s) {
+  float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+  float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+  for (int c = 12; c + 8 <= 124; c += 8) {
+    m0 = fmax3(m0, s[c], s[c + 1]);
+    m1 = fmax3(m1, s[c + 2], s[c + 3]);
+    m2 = fmax3(m2, s[c + 4], s[c + 5]);
+    m3 = fmax3(m3, s[c + 6], s[c + 7]);
+  }
+  m0 = fmax3(m0, s[124], s[125]);
+  m1 = fmax3(m1, s[126], s[127]);
+  return fmax3(fmaxf(m0, m1), m2, m3);
+}
+
 // Register rebalancing between warpgroups (all warps of a warpgroup execute it).
 template <int R>
 __device__ __forceinline__ void setmaxnreg_inc() {
