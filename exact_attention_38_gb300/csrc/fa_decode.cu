@@ -298,11 +298,25 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
         tmem_ld32(s_tm + 64u * hf, sr);
         tmem_ld32(s_tm + 64u * hf + 32u, sr + 32);
         tmem_wait_ld();
+        float* v = reinterpret_cast<float*>(sr);
+        if (masked) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float v = (masked && 64 * hf + c >= nvis) ? -INFINITY : __uint_as_float(sr[c]);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < 64; ++c)
+            if (64 * hf + c >= nvis) v[c] = -INFINITY;
         }
+        // four independent chains of three-input maxima
+        float m0 = fmax3(mx, v[0], v[1]), m1 = fmax3(v[2], v[3], v[4]), m2 = fmax3(v[5], v[6], v[7]);
+        float m3 = fmax3(v[8], v[9], v[10]);
+#pragma unroll
+        for (int c = 11; c + 8 <= 59; c += 8) {
+          m0 = fmax3(m0, v[c], v[c + 1]);
+          m1 = fmax3(m1, v[c + 2], v[c + 3]);
+          m2 = fmax3(m2, v[c + 4], v[c + 5]);
+          m3 = fmax3(m3, v[c + 6], v[c + 7]);
+        }
+        m0 = fmax3(m0, v[59], v[60]);
+        m1 = fmax3(m1, v[61], v[62]);
+        mx = fmax3(fmax3(m0, m1, m2), m3, v[63]);
       }
       if (j == 0) {
         m = mx;
@@ -325,6 +339,7 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
       }
       // a row with no visible key so far keeps m = -inf and gets p = 0
       const float neg = (m == -INFINITY) ? 0.f : -m * cl2;
+      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg);
       float sum = 0.f;
       // P of half hf goes to packed columns [32 hf, 32 hf + 32), over S columns this
       // thread has already read (half 1's scores, columns 64-127, are untouched by it)
@@ -335,16 +350,21 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
         tmem_ld32(s_tm + 64u * hf + 32u, sr + 32);
         tmem_wait_ld();
         uint32_t pk[32];
+        uint64_t acc = 0ull;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int c = 64 * hf + 2 * u;
           const float s0 = (masked && c >= nvis) ? -INFINITY : __uint_as_float(sr[2 * u]);
           const float s1 = (masked && c + 1 >= nvis) ? -INFINITY : __uint_as_float(sr[2 * u + 1]);
-          const float p0 = dec_ex2(fmaf(s0, cl2, neg));
-          const float p1 = dec_ex2(fmaf(s1, cl2, neg));
-          sum += p0 + p1;
+          float a0, a1;
+          f2unpack(ffma2(f2pack(s0, s1), cl2x2, negx2), a0, a1);
+          const float p0 = dec_ex2(a0), p1 = dec_ex2(a1);
+          acc = fadd2(acc, f2pack(p0, p1));
           pk[u] = dec_pack2<BF16>(p0, p1);
         }
+        float sa, sb;
+        f2unpack(acc, sa, sb);
+        sum += sa + sb;
         tmem_st32(s_tm + 32u * hf, pk);
       }
       l += sum;
