@@ -195,18 +195,29 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU baseline
 
-def cpu_oracle_sample(w, steps=1):
-    """The fp64 oracle, as it stands, on a bounded slice of the same workload."""
+def cpu_oracle_sample(w, steps=1, target_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded slice of the same workload: the first
+    n_s positions of `heads` heads, sized from a short calibration run so one step takes
+    about `target_s` seconds of host time (at most the workload's N and Hq)."""
     import numpy as np
 
     import oracle
     from exact_attention_38_gb300.inputs import make_inputs, to_f64
 
     cores = len(os.sched_getaffinity(0))
-    n_s, heads = min(w["N"], 4096), min(w["Hq"], 4)
+    scale = 1.0 / math.sqrt(w["d"])
+    # calibration: one head, 1024 positions (the oracle's cost grows as heads * N^2)
+    n_c = min(w["N"], 1024)
+    xc = {k: to_f64(v) for k, v in make_inputs(1, n_c, 1, 1, w["d"], dtype=w["dtype"], seed=4).items()}
+    t0 = time.perf_counter()
+    oracle.attn_bwd_ref(xc["q"], xc["k"], xc["v"], xc["do"], w["causal"], scale)
+    per_head_c = max(time.perf_counter() - t0, 1e-4)
+    n_s = w["N"]
+    while n_s > n_c and per_head_c * (n_s / n_c) ** 2 > target_s:
+        n_s //= 2
+    heads = int(max(1, min(w["Hq"], round(target_s / (per_head_c * (n_s / n_c) ** 2)))))
     x = make_inputs(1, n_s, heads, heads, w["d"], dtype=w["dtype"], seed=3)
     xo = {k: to_f64(v) for k, v in x.items()}
-    scale = 1.0 / math.sqrt(w["d"])
     fl = 3.5 * 4.0 * heads * n_s ** 2 * w["d"] * (0.5 if w["causal"] else 1.0)
     times = []
     for _ in range(steps):
@@ -215,7 +226,8 @@ def cpu_oracle_sample(w, steps=1):
         times.append(time.perf_counter() - t0)
         assert np.isfinite(r["dq"]).all()
     sample = (f"oracle attn_bwd_ref (fwd+all grads, fp64 numpy) on B=1, {heads} heads, N={n_s}, d={w['d']} "
-              f"({'causal' if w['causal'] else 'non-causal'}); FLOPs by the same formula")
+              f"({'causal' if w['causal'] else 'non-causal'}), sized for ~{target_s:.0f} s per step; FLOPs by the "
+              f"same formula")
     return fl, times, cores, sample
 
 
@@ -224,7 +236,9 @@ def run_reference(a):
     if rank != 0:
         return
     w = workload(a)
-    fl, times, cores, sample = cpu_oracle_sample(w, steps=a.warmup + a.steps)
+    # every step a bounded sample, sized so the whole run stays within about two minutes
+    per_step = max(0.5, min(12.0, 120.0 / max(1, a.warmup + a.steps)))
+    fl, times, cores, sample = cpu_oracle_sample(w, steps=a.warmup + a.steps, target_s=per_step)
     t = times[a.warmup:] if len(times) > a.warmup else times
     sec = sum(t) / len(t)
     val = fl / sec / 1e12
