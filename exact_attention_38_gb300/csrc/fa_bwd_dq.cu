@@ -11,15 +11,18 @@
 // ("FlashAttention-2: atención eficiente en GPU para contextos largos", section "Bloques
 // pequeños, normalización global"): dS = P * (dP - D), P = exp(s - lse).
 //
-// GB300 form (one 128-query tile per CTA, 256 threads):
-//  * warp 4 streams Q and dO once and K_j / V_j through a ring (128-byte swizzle);
-//  * warp 5 issues S_j = Q K_j^T into one of two TMEM buffers and dP_j = dO V_j^T, then
-//    dQ += dS_{j-1} K_{j-1} with dS read from TMEM, where the softmax warpgroup left it
-//    as 16-bit pairs over S; S double-buffered so S_{j+1} and dP_{j+1} overlap the
-//    softmax of block j;
-//  * warpgroup 0 (thread = query row = TMEM lane) turns S_j, dP_j into
-//    dS = exp2(s * scale * log2 e - lse * log2 e) * (dP - D) in two 64-column halves;
-//  * epilogue: dQ * scale rounded to 16 bits, stored row by row.
+// GB300 form (one 128-query tile per CTA, 384 threads):
+//  * warp 8 streams Q and dO once and K_j / V_j through a ring (128-byte swizzle);
+//  * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers and dP_j = dO V_j^T, then
+//    dQ += dS_{j-1} K_{j-1} with dS read from TMEM, where the dS warpgroups left it as
+//    16-bit pairs over S; S double-buffered so S_{j+1} and dP_{j+1} overlap the dS work
+//    of block j;
+//  * warpgroups 0 and 1 (thread = query row = TMEM lane) each take 64 of the block's 128
+//    keys and turn S_j, dP_j into dS = exp2(s * scale * log2 e - lse * log2 e) * (dP - D),
+//    written over the columns of S they read (keys 0-63 packed at columns 0-31, keys
+//    64-127 at columns 64-95);
+//  * epilogue: dQ * scale rounded to 16 bits, stored row by row (each warpgroup half of
+//    the head dimension).
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -34,7 +37,7 @@ struct DqCfg {
   static constexpr int TILE_BYTES = 128 * D * 2;  // Q, dO, or one K / V block of 128 rows
   static constexpr int CHUNK_BYTES = 128 * 128;
   static constexpr int STAGES = (D == 128) ? 4 : 8;
-  static constexpr int THREADS = 256;
+  static constexpr int THREADS = 384;
   // barriers: q_full, s_full[2], dp_free, ds_ready[2], dq_done, final, kv_full[S], kv_empty[S]
   static constexpr int NBARS = 8 + 2 * STAGES;
   static constexpr int SMEM = 1024 + (2 + STAGES) * TILE_BYTES + 8 * NBARS + 64;
@@ -60,7 +63,7 @@ __device__ __forceinline__ uint32_t dq_pack2(float lo, float hi) {
 }
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw_dq[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_dq) + 1023) & ~uintptr_t(1023));
@@ -106,9 +109,9 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(q_full, 1);
     mbar_init(s_full(0), 1);
     mbar_init(s_full(1), 1);
-    mbar_init(dp_free, 128);
-    mbar_init(ds_ready(0), 128);
-    mbar_init(ds_ready(1), 128);
+    mbar_init(dp_free, 256);
+    mbar_init(ds_ready(0), 256);
+    mbar_init(ds_ready(1), 256);
     mbar_init(dq_done, 1);
     mbar_init(final_bar, 1);
     for (int st = 0; st < C::STAGES; ++st) {
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
     }
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -132,9 +135,10 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
   };
   constexpr unsigned FULL = 0xffffffffu;
 
-  if (warp >= 4) {
+  if (warp >= 8) {
+    setmaxnreg_dec<80>();
     const bool leader = elect_one();
-    if (warp == 4) {
+    if (warp == 8) {
       // ------------------------------------------------------------ TMA producer
       if (leader) {
         tma_prefetch_desc(&p.tm_q);
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
         mbar_wait(q_full, 0, nullptr, lim);
       }
       __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t bf = BF16 ? 1u : 0u;
       constexpr uint32_t id_sq = idesc_f16(128, 128, bf, 0, 0);  // S, dP: both operands K-major
@@ -198,11 +202,6 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
             ok = false;
             break;
           }
-          // dP_j overwrites dP_{j-1}: the softmax warpgroup must have read it
-          if (j > 0 && !__all_sync(FULL, mbar_wait(dp_free, (j - 1) & 1, abort_flag, lim))) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const uint32_t s_tm = tbase + C::T_S + 128u * (j & 1);
           if (leader) {
@@ -213,6 +212,14 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
               const uint64_t o = u16((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32);
               mma_ss(s_tm, dq0 + o, dkv0 + u16(ks * C::TILE_BYTES) + o, id_sq, kk > 0 ? 1u : 0u);
             }
+          }
+          // dP_j overwrites dP_{j-1}: the dS warpgroups must have read it
+          if (j > 0 && !__all_sync(FULL, mbar_wait(dp_free, (j - 1) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (leader) {
             // dP_j = dO V_j^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -231,12 +238,14 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
           }
           tc_fence_after();
           if (leader) {
-            // dQ += dS_i K_i: dS from TMEM (16-bit pairs over S_i's buffer), K_i MN-major
+            // dQ += dS_i K_i: dS from TMEM (16-bit pairs over S_i's buffer: keys 0-63 at
+            // columns 0-31, keys 64-127 at columns 64-95), K_i MN-major
             const uint32_t ds_tm = tbase + C::T_S + 128u * (i & 1);
             const uint64_t kd = dk_mn0 + u16(ks * C::TILE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tbase + C::T_DQ, ds_tm + 8u * kk, kd + u16(kk * 2048), id_dq, (i > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tbase + C::T_DQ, ds_tm + 64u * (kk / 4) + 8u * (kk % 4), kd + u16(kk * 2048), id_dq,
+                     (i > 0 || kk > 0) ? 1u : 0u);
             mma_commit(kv_empty(ks));
             if (i == n - 1) mma_commit(dq_done);
           }
@@ -253,10 +262,12 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
       __syncwarp();
     }
   } else {
-    // ------------------------------------------------------------ dS warpgroup
-    const int r = warp * 32 + lane;
+    setmaxnreg_inc<200>();
+    // ----------------------------------------------------------- dS warpgroups
+    const int hf = warp >> 2;  // keys [64 hf, 64 hf + 64) of each block
+    const int r = (warp & 3) * 32 + lane;
     const int row = r0 + r;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const float cl2 = p.scale_log2;
     // -lse * log2(e) and -D of this query row, from the preprocess (-inf and 0 past N)
     const long long vrow = static_cast<long long>(bh) * p.Npad + row;
@@ -272,33 +283,36 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
       const uint32_t s_tm = tbase + lane_off + C::T_S + 128u * (j & 1);
       const uint32_t dp_tm = tbase + lane_off + C::T_DP;
       const int nvis = CAUSAL && j == n - 1 ? row + 1 - 128 * j : 128;  // diagonal block
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      {
         uint32_t sv[64], dpv[64];
         tmem_ld32(s_tm + 64u * hf, sv);
         tmem_ld32(s_tm + 64u * hf + 32u, sv + 32);
         tmem_ld32(dp_tm + 64u * hf, dpv);
         tmem_ld32(dp_tm + 64u * hf + 32u, dpv + 32);
         tmem_wait_ld();
-        if (hf == 1) {
-          tc_fence_before();
-          mbar_arrive(dp_free);  // both halves of dP_j are in registers
-        }
+        tc_fence_before();
+        mbar_arrive(dp_free);  // this warpgroup's half of dP_j is in registers
+        const uint64_t cl2x2 = f2pack(cl2, cl2), nl2x2 = f2pack(nl2, nl2), ndx2 = f2pack(nd, nd);
         uint32_t pk[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int c = 64 * hf + 2 * u;
-          float p0 = dq_ex2(fmaf(__uint_as_float(sv[2 * u]), cl2, nl2));
-          float p1 = dq_ex2(fmaf(__uint_as_float(sv[2 * u + 1]), cl2, nl2));
+          float a0, a1;
+          f2unpack(ffma2(f2pack(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1])), cl2x2, nl2x2), a0, a1);
+          float p0 = dq_ex2(a0), p1 = dq_ex2(a1);
           if (CAUSAL) {
             if (c >= nvis) p0 = 0.f;
             if (c + 1 >= nvis) p1 = 0.f;
           }
-          pk[u] = dq_pack2<BF16>(p0 * (__uint_as_float(dpv[2 * u]) + nd), p1 * (__uint_as_float(dpv[2 * u + 1]) + nd));
+          float d0, d1;
+          f2unpack(fmul2(f2pack(p0, p1),
+                         fadd2(f2pack(__uint_as_float(dpv[2 * u]), __uint_as_float(dpv[2 * u + 1])), ndx2)),
+                   d0, d1);
+          pk[u] = dq_pack2<BF16>(d0, d1);
         }
-        // dS of half hf -> packed columns [32 hf, 32 hf + 32) of S_j's buffer (S columns
-        // this thread has already read)
-        tmem_st32(s_tm + 32u * hf, pk);
+        // dS of this half -> 32 packed columns at the start of the half's own S columns
+        // (already read by this thread; the other warpgroup reads only its own half)
+        tmem_st32(s_tm + 64u * hf, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -309,12 +323,12 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
       *wg_fail = 1;
       fail();
     }
-    named_bar_sync_n(1, 128);
-    if (*wg_fail == 0) {  // uniform across the warpgroup
+    named_bar_sync_n(1, 256);
+    if (*wg_fail == 0) {  // uniform across both warpgroups
       tc_fence_after();
       uint16_t* out = p.dq + ((static_cast<long long>(b) * N + row) * p.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {  // this warpgroup's half of d
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::T_DQ + 32u * c, v);  // all lanes (.sync.aligned)
         tmem_wait_ld();
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(256, 1) fa_bwd_dq_kernel(const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
