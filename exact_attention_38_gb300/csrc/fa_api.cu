@@ -534,7 +534,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   p.N = N;
   p.score_scale = scale * q_descale * k_descale;
   p.score_log2 = p.score_scale * 1.4426950408889634f;
-  p.out_scale = v_descale / 256.0f;
+  p.out_scale = v_descale;  // P and l both carry the 2^8 pre-scale, which cancels in O / l
   p.wait_limit_ns = kWaitLimitNs;
   const cudaError_t e = launch_fwd_fp8(p, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -11,8 +11,9 @@
 // by 2^8 before its E4M3 rounding (its largest element per row is 1, so the scaled
 // values stay below E4M3's 448 while values down to about 2^-17 keep a representable
 // step; the lazy rescale therefore lets the running maximum lag by at most 0.5 in log2
-// units instead of 8) and O is divided by 2^8 l and multiplied by v's descale in the
-// epilogue; O is written in bf16, lse in fp32.
+// units instead of 8).  The 2^8 is added to the exponent, and the row sum l carries it
+// too, so O / l needs no extra factor; O is multiplied by v's descale and written in
+// bf16, lse (fp32) subtracts 8 ln 2.
 //
 // GB300 form: the 16-bit forward's pipeline (two 128-row query tiles per CTA, a TMA
 // warp, an MMA warp, one softmax warpgroup per tile, P from tensor memory) with
@@ -35,7 +36,7 @@ constexpr int kStages = 8;        // K / V^T ring
 constexpr int kThreads = 384;
 constexpr int kNbars = 8 + 2 * kStages + 1;
 constexpr int kSmem = 1024 + 2 * kTile + kStages * kTile + 8 * kNbars + 64;
-constexpr float kPScale = 256.f;  // P is rounded to E4M3 as P * 2^8
+constexpr float kLn2 = 0.69314718055994531f;  // P is rounded to E4M3 as P * 2^8
 // Lazy rescale threshold (log2 units).  With a stale maximum p can reach 2^tau, so
 // 2^8 * 2^tau must stay below E4M3's largest value 448: tau = 0.5 keeps P * 2^8 <= 362
 // (the 16-bit kernel's 8 would saturate).
@@ -329,8 +330,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         }
         tmem_wait_st();
       }
-      const float neg = -m * cl2;
-      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg), ps2 = f2pack(kPScale, kPScale);
+      // the 2^8 pre-scale of P is folded into the exponent: p = exp2(s c - m c + 8); l
+      // sums the scaled values too, so it cancels in O / l (and lse subtracts 8 ln 2)
+      const float neg = -m * cl2 + 8.0f;
+      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg);
       uint64_t acc0 = 0ull, acc1 = 0ull;
       uint32_t pk[32];
 #pragma unroll
@@ -342,8 +345,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         acc0 = fadd2(acc0, p01);
         acc1 = fadd2(acc1, p23);
         float q0, q1, q2, q3;
-        f2unpack(fmul2(p01, ps2), q0, q1);
-        f2unpack(fmul2(p23, ps2), q2, q3);
+        f2unpack(p01, q0, q1);
+        f2unpack(p23, q2, q3);
         pk[c4] = pack4_e4m3(q0, q1, q2, q3);
       }
       float sa, sb, sc2, sd;
@@ -382,7 +385,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
             *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = w;
           }
         }
-        if (row < N) p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] = m * p.score_scale + logf(l);
+        if (row < N)
+          p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] = m * p.score_scale + logf(l) - 8.0f * kLn2;
       }
     }
   }

@@ -106,7 +106,7 @@ struct Fp8Params {
   int B, Hq, Hkv, N, Npad;  // Npad = N rounded up to 128
   float score_log2;         // scale * q_descale * k_descale * log2(e)
   float score_scale;        // scale * q_descale * k_descale
-  float out_scale;          // v_descale / 2^8 (P is rounded to E4M3 as P * 2^8)
+  float out_scale;          // v_descale (P and its row sum both carry a 2^8 pre-scale)
   uint64_t wait_limit_ns;
 };
 cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream);
