@@ -441,7 +441,9 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
                 tma_store_4d(&p.tm_o, smem_u32(stage + ch * C::CHUNK_BYTES), ch * 64, h, r0_of(t), b);
             }
             bulk_commit_group();
-            bulk_wait_group0();
+            // the staging (Q_t's buffer) must outlive the copy's reads of it; the global
+            // writes need no wait (they complete before the kernel does)
+            bulk_wait_group_read0();
           }
         }
         if (row < len_q) {
