@@ -130,29 +130,40 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
   const int sub = lane / LPR, part = lane % LPR;
   const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  for (long long base = wid * (32 / LPR); base < rows; base += warps_total * (32 / LPR)) {
-    const long long r = base + sub;
-    float acc = 0.f;
-    if (r < rows) {
-      const uint4 a = *reinterpret_cast<const uint4*>(p.o + r * D + part * 8);
-      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + r * D + part * 8);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+  // each warp keeps kGroups row groups of loads in flight before it reduces any
+  constexpr int RPW = 32 / LPR, kGroups = 4;
+  for (long long base = wid * RPW * kGroups; base < rows; base += warps_total * RPW * kGroups) {
+    uint4 a[kGroups], g[kGroups];
+#pragma unroll
+    for (int u = 0; u < kGroups; ++u) {
+      const long long r = base + u * RPW + sub;
+      a[u] = g[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) {
+        a[u] = *reinterpret_cast<const uint4*>(p.o + r * D + part * 8);
+        g[u] = *reinterpret_cast<const uint4*>(p.dout + r * D + part * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroups; ++u) {
+      const long long r = base + u * RPW + sub;
+      const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, gv[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      float acc = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         acc += bw_unpack_lo<BF16>(av[i]) * bw_unpack_lo<BF16>(gv[i]) +
                bw_unpack_hi<BF16>(av[i]) * bw_unpack_hi<BF16>(gv[i]);
-    }
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (r < rows && part == 0) {
-      // r = (b*N + n)*Hq + h
-      const int h = static_cast<int>(r % p.Hq);
-      const long long bn = r / p.Hq;
-      const int n = static_cast<int>(bn % p.N);
-      const int b = static_cast<int>(bn / p.N);
-      const long long bh = static_cast<long long>(b) * p.Hq + h;
-      p.dvec[bh * p.Npad + n] = -acc;
-      p.l2vec[bh * p.Npad + n] = -p.lse[bh * p.N + n] * kLog2e;
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (r < rows && part == 0) {
+        // r = (b*N + n)*Hq + h
+        const int h = static_cast<int>(r % p.Hq);
+        const long long bn = r / p.Hq;
+        const int n = static_cast<int>(bn % p.N);
+        const int b = static_cast<int>(bn / p.N);
+        const long long bh = static_cast<long long>(b) * p.Hq + h;
+        p.dvec[bh * p.Npad + n] = -acc;
+        p.l2vec[bh * p.Npad + n] = -p.lse[bh * p.N + n] * kLog2e;
+      }
     }
   }
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -240,6 +251,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
     row0 = sq;
   }
   const float* src = p.dq_acc + static_cast<long long>(bh) * D * p.Npad + n0;
+#pragma unroll 8
   for (int i = threadIdx.x; i < D * 64; i += 256) {
     const int dd = i >> 6, n = i & 63;
     tile[dd][n] = src[static_cast<long long>(dd) * p.Npad + n];
