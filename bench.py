@@ -195,6 +195,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU baseline
 
+def host_cpu():
+    """Host CPU description for the baseline record (architecture and model, if known)."""
+    import platform
+
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return f"{platform.machine()} {model}".strip()
+
+
 def cpu_oracle_sample(w, steps=1, target_s=12.0):
     """The fp64 oracle, as it stands, on a bounded slice of the same workload: the first
     n_s positions of `heads` heads, sized from a short calibration run so one step takes
@@ -247,7 +264,8 @@ def run_reference(a):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(w, "step") + " [oracle runs a bounded slice, see cpu_baseline]",
                        "parallelism": "host cores"},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             "cpu": host_cpu(), "seconds_per_step": sec},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -391,7 +409,7 @@ def run_native(a):
     if not a.no_cpu_baseline:
         fl_s, times, cores, sample = cpu_oracle_sample(w, steps=1)
         cpu = {"value": fl_s / times[0] / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": sample, "seconds": times[0]}
+               "sample": sample, "seconds": times[0], "cpu": host_cpu()}
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": a.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
