@@ -37,6 +37,12 @@
  *    work is enqueued.  Errors inside a kernel (a bounded wait that ran out) are
  *    recorded in a per-device error word that fa_check_device_error() reads.
  *  - Calls on different streams may overlap; the library keeps no per-call state.
+ *  - The compute entry points may be captured into a CUDA graph and replayed (their
+ *    host-side work, tensor-map encoding and launch attributes, happens at capture and
+ *    is baked into the graph's kernel parameters; the buffers must then stay at the
+ *    captured addresses).  Make one call on the device before capturing: the first
+ *    call looks up the device's error word.  fa_check_device_error synchronises and
+ *    cannot be captured.
  */
 #ifndef FA_H_
 #define FA_H_
