@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="decode forward: --B sequences (default 8) of --N cached keys (default 16384), "
                          "--Nq new queries, Hq=--H (default 32 here), Hkv=--Hkv (default 8 here)")
+    ap.add_argument("--paged", action="store_true",
+                    help="with --decode: the caches as 128-row pages in a shuffled order behind a block table")
     ap.add_argument("--fp8", action="store_true",
                     help="forward only with E4M3 q, k, v (per-tensor descales), bf16 output")
     ap.add_argument("--Nq", type=int, default=1)
@@ -606,6 +608,32 @@ def run_decode(a):
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd_decode")
 
+    if a.paged:
+        # the same caches cut into 128-row pages stored in a shuffled order
+        P = (N + 127) // 128
+        g = torch.Generator().manual_seed(5)
+        perm = torch.randperm(B * P, generator=g).to(dev)
+        table = perm.view(B, P).to(torch.int32).contiguous()
+
+        def to_pages(c):
+            padded = torch.zeros((B, P * 128, Hkv, d), dtype=c.dtype, device=dev)
+            padded[:, :N] = c
+            pages = torch.empty((B * P, 128, Hkv, d), dtype=c.dtype, device=dev)
+            pages[perm] = padded.view(B * P, 128, Hkv, d)
+            return pages
+
+        kp, vp = to_pages(k), to_pages(v)
+        del k, v
+        ws_bytes = fa.fa_decode_workspace_size(B, Hq, Hkv, Nq, P * 128, d, a.splits)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+        def step():  # noqa: F811
+            st = fa.fa_fwd_decode_paged(q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(), cl.data_ptr(),
+                                        o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, B * P, P, d, causal, scale,
+                                        a.splits, fa.FA_BF16, ws.data_ptr(), ws_bytes, sp)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_fwd_decode_paged")
+
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
@@ -634,7 +662,7 @@ def run_decode(a):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"exact attention decode forward: B={B} sequences x {N} cached keys, Nq={Nq} new "
                                    f"queries, Hq={Hq} Hkv={Hkv} d={d} bf16 {'causal' if causal else 'non-causal'}, "
-                                   f"{S} key splits",
+                                   f"{S} key splits{', paged cache (128-row pages, shuffled)' if a.paged else ''}",
                        "l2": "flushed between steps (outside the timed events); the cache exceeds L2"},
             "tflops": tflops,
             "roofline": {"bound": "hbm", "kernel": "fa_decode_kernel (+ fa_decode_combine)", "achieved": gbs,

@@ -540,6 +540,57 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                              const int* cache_seqlens, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                              int num_pages, int max_pages, int d, int causal, float scale, int num_splits,
+                              fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID;
+  if (!aligned4(cache_seqlens) || !aligned4(block_table)) return FA_ERR_INVALID;
+  if (num_pages < 1 || max_pages < 1) return FA_ERR_INVALID;
+  if (max_pages > (1 << 24) / 128) return FA_ERR_UNSUPPORTED;
+  const int Nmax = max_pages * 128;
+  const fa_status st = check_decode(B, Hq, Hkv, Nq, Nmax, d, scale, static_cast<int>(dtype), num_splits);
+  if (st != FA_OK) return st;
+  if (static_cast<long long>(num_pages) * 128 * Hkv * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, Nq, Nmax, d, num_splits);
+  if (ws.total > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                       workspace_bytes < ws.total))
+    return FA_ERR_INVALID;
+  const int G = Hq / Hkv;
+  DecParams p{};
+  if (!encode_bshd_box_map(&p.tm_q, q, B, Nq, Hq, d, G, Nq, dtype) ||
+      !encode_bshd_map(&p.tm_k, k_pages, num_pages, 128, Hkv, d, 128, dtype) ||
+      !encode_bshd_map(&p.tm_v, v_pages, num_pages, 128, Hkv, d, 128, dtype))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  p.seqlens_k = cache_seqlens;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.opart = ws.total ? reinterpret_cast<float*>(w + ws.opart_off) : nullptr;
+  p.lpart = ws.total ? reinterpret_cast<float*>(w + ws.lpart_off) : nullptr;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nmax = Nmax;
+  p.G = G;
+  p.M = G * Nq;
+  p.S = sp.S;
+  p.cps = sp.cps;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_decode(p, d, dtype, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_selftest_wait_timeout(int limit_us, fa_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID;
   unsigned* err = device_error_word();

@@ -186,9 +186,18 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
           if (leader) {
             mbar_arrive_expect_tx(kv_full(slot), C::TILE_BYTES);
             const CUtensorMap* map = kind ? &p.tm_v : &p.tm_k;
+            // contiguous cache: rows 128 (jb0 + j) of sequence b; paged cache: all 128 rows
+            // of the block's page (a page index outside the cache reads zeros and is
+            // reported)
+            int row = 128 * (jb0 + j), outer = b;
+            if (p.block_table != nullptr) {
+              outer = p.block_table[static_cast<long long>(b) * p.max_pages + jb0 + j];
+              row = 0;
+              if (kind == 0 && (outer < 0 || outer >= p.num_pages)) atomicOr(p.err, kDevErrSeqlens);
+            }
             for (int ch = 0; ch < C::CHUNKS; ++ch)
               tma_load_4d(smem_u32(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES), map, kv_full(slot), ch * 64,
-                          hkv, 128 * (jb0 + j), b);
+                          hkv, row, outer);
           }
         }
       }

@@ -79,8 +79,11 @@ struct BwdParams {
 // Decode-shaped forward with split keys.
 struct DecParams {
   CUtensorMap tm_q;        // 4-D over q [B, Nq, Hq, d], box {64, G, Nq, 1}: the group's rows
-  CUtensorMap tm_k, tm_v;  // 4-D over the caches [B, Nmax, Hkv, d], box {64, 1, 128, 1}
+  CUtensorMap tm_k, tm_v;  // 4-D over the caches [B, Nmax, Hkv, d] (paged: [num_pages, 128, Hkv, d]),
+                           // box {64, 1, 128, 1}
   const int* seqlens_k;    // [B] keys in the cache of each sequence (device)
+  const int* block_table;  // paged caches: [B, max_pages] page of each 128-key block (device); else null
+  int max_pages, num_pages;
   uint16_t* o;             // [B, Nq, Hq, d]
   float* lse;              // [B, Hq, Nq]
   float* opart;            // splits > 1: [B*Hkv*S, M, d] normalised partial outputs (fp32)

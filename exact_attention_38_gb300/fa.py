@@ -56,6 +56,8 @@ def _load():
     lib.fa_bwd_varlen_workspace_size.restype = sz
     lib.fa_fwd_decode.argtypes = [vp] * 6 + [i] * 7 + [f, i, i, vp, sz, vp]
     lib.fa_fwd_decode.restype = i
+    lib.fa_fwd_decode_paged.argtypes = [vp] * 7 + [i] * 8 + [f, i, i, vp, sz, vp]
+    lib.fa_fwd_decode_paged.restype = i
     lib.fa_decode_workspace_size.argtypes = [i] * 7
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode_num_splits.argtypes = [i] * 7
@@ -135,6 +137,14 @@ def fa_fwd_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, Nq, Nm
     """Mirror of the C ``fa_fwd_decode``."""
     return lib.fa_fwd_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, Nq, Nmax, d, int(causal),
                              float(scale), int(num_splits), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_decode_paged(q, k_pages, v_pages, block_table, cache_seqlens, o, lse, B, Hq, Hkv, Nq, num_pages,
+                        max_pages, d, causal, scale, num_splits, dtype, workspace, workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_fwd_decode_paged``."""
+    return lib.fa_fwd_decode_paged(q, k_pages, v_pages, block_table, cache_seqlens, o, lse, B, Hq, Hkv, Nq, num_pages,
+                                   max_pages, d, int(causal), float(scale), int(num_splits), int(dtype), workspace,
+                                   int(workspace_bytes), stream)
 
 
 def fa_decode_workspace_size(B, Hq, Hkv, Nq, Nmax, d, num_splits=0) -> int:
@@ -324,6 +334,32 @@ def forward_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=No
                     k_descale, v_descale, _ptr(workspace), workspace.numel(), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_fp8")
+    return o, lse
+
+
+def forward_decode_paged(q, k_pages, v_pages, block_table, cache_seqlens, causal=False, scale=None, num_splits=0,
+                         out=None, lse=None, workspace=None, stream=None):
+    """Decode forward over a paged cache: k_pages / v_pages [num_pages, 128, Hkv, d],
+    block_table int32 CUDA [B, max_pages].  Returns (o [B,Nq,Hq,d], lse [B,Hq,Nq])."""
+    B, Nq, Hq, d = q.shape
+    num_pages, page, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if page != 128 or v_pages.shape != k_pages.shape or k_pages.shape[3] != d:
+        raise ValueError("pages must be [num_pages, 128, Hkv, d] for both caches")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    max_pages = block_table.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = fa_decode_workspace_size(B, Hq, Hkv, Nq, max_pages * 128, d, num_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = fa_fwd_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(cache_seqlens), _ptr(o),
+                             _ptr(lse), B, Hq, Hkv, Nq, num_pages, max_pages, d, causal, scale, num_splits,
+                             _DT[q.dtype], _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                             _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_decode_paged")
     return o, lse
 
 

@@ -212,6 +212,22 @@ fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
                         fa_stream_t stream);
 
 /*
+ * fa_fwd_decode over a paged cache: the keys and values of all sequences live in pages
+ * of 128 rows, k_pages / v_pages [num_pages, 128, Hkv, d], and block_table (DEVICE int32
+ * [B, max_pages]) gives the page holding keys [128 j, 128 j + 128) of sequence b at
+ * block_table[b * max_pages + j].  Entries past a sequence's last block are not read.
+ * cache_seqlens[b] <= max_pages * 128.  Other arguments, results and workspace as
+ * fa_fwd_decode with Nmax = max_pages * 128 (use fa_decode_workspace_size with that
+ * Nmax).  A page index outside [0, num_pages) reads zeros and is reported as
+ * FA_ERR_INVALID by the next fa_check_device_error().  Serving engines keep caches this
+ * way so that sequences grow without moving memory; the pages describe no paging.
+ */
+fa_status fa_fwd_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                              const int* cache_seqlens, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                              int num_pages, int max_pages, int d, int causal, float scale, int num_splits,
+                              fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_bwd with a fixed summation order: the same arguments, results within the same
  * tolerance, and dq, dk, dv identical bit for bit from run to run (fa_bwd's dq depends
  * on the order in which key blocks land their fp32 additions).  The dK/dV kernel runs

@@ -194,6 +194,35 @@ def test_decode_argument_errors_need_no_device(lib, kw, code):
     assert _decode(lib, **kw) == code
 
 
+def _decode_paged(lib, **kw):
+    a = dict(q=0x10000, kp=0x20000, vp=0x30000, table=0x70000, cl=0x40000, o=0x50000, lse=0x60000, B=2, Hq=8, Hkv=2,
+             Nq=1, num_pages=64, max_pages=32, d=128, causal=1, scale=0.088, splits=0, dtype=0, ws=0x100000,
+             ws_bytes=None)
+    a.update(kw)
+    i = ctypes.c_int
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.fa_decode_workspace_size.argtypes = [i] * 7
+    need = lib.fa_decode_workspace_size(a["B"], a["Hq"], a["Hkv"], a["Nq"], 128 * a["max_pages"], a["d"],
+                                        a["splits"])
+    ws_bytes = need if a["ws_bytes"] is None else a["ws_bytes"]
+    vp = ctypes.c_void_p
+    f = lib.fa_fwd_decode_paged
+    f.argtypes = [vp] * 7 + [i] * 8 + [ctypes.c_float, i, i, vp, ctypes.c_size_t, vp]
+    f.restype = i
+    return f(a["q"], a["kp"], a["vp"], a["table"], a["cl"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Nq"],
+             a["num_pages"], a["max_pages"], a["d"], a["causal"], a["scale"], a["splits"], a["dtype"], a["ws"],
+             ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), 1), (dict(table=0x70002), 1), (dict(kp=0x20008), 1), (dict(cl=None), 1),
+    (dict(num_pages=0), 1), (dict(max_pages=0), 1), (dict(max_pages=1 << 20), 2), (dict(Hq=6, Hkv=4), 1),
+    (dict(d=256), 2), (dict(ws_bytes=16), 1), (dict(scale=float("nan")), 1),
+])
+def test_decode_paged_argument_errors_need_no_device(lib, kw, code):
+    assert _decode_paged(lib, **kw) == code
+
+
 def test_decode_split_count_and_workspace(lib):
     i = ctypes.c_int
     lib.fa_decode_num_splits.restype = i

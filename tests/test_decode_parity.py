@@ -73,3 +73,61 @@ def test_length_out_of_range_is_reported(fa_lib):
         fa.check_device_error()
     assert e.value.status == fa.FA_ERR_INVALID
     assert torch.isnan(o[1]).all() and not torch.isnan(o[0]).any()
+
+
+def _paged(x, B, Nmax, lens, seed):
+    """Scatter the contiguous caches into 128-row pages in a shuffled order: returns
+    k_pages, v_pages [num_pages, 128, Hkv, d] and the block table [B, max_pages]."""
+    max_pages = (Nmax + 127) // 128
+    num_pages = B * max_pages + 3  # a few pages nobody uses
+    perm = np.random.default_rng(seed).permutation(num_pages)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    shape = (num_pages, 128) + tuple(x["k"].shape[2:])
+    kp = torch.zeros(shape, dtype=x["k"].dtype)
+    vp = torch.zeros(shape, dtype=x["v"].dtype)
+    n = 0
+    for b in range(B):
+        for j in range((lens[b] + 127) // 128):
+            pg = int(perm[n])
+            n += 1
+            table[b, j] = pg
+            rows = min(128, Nmax - 128 * j)
+            kp[pg, :rows] = x["k"][b, 128 * j:128 * j + rows]
+            vp[pg, :rows] = x["v"][b, 128 * j:128 * j + rows]
+    return kp, vp, torch.from_numpy(table)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("num_splits", [0, 1, 5])
+def test_paged_cache_matches_contiguous(fa_lib, causal, num_splits):
+    """The paged cache gives the same bits as the contiguous one (the same products in the
+    same order, only the K/V tile addresses differ), and both agree with the oracle."""
+    fa = fa_lib
+    B, Nq, Nmax, Hq, Hkv, d = 3, 2, 1200, 8, 2, 128
+    lens = [1200, 1, 640]
+    x = make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype="bf16", seed=46)
+    kp, vp, table = _paged(x, B, Nmax, lens, seed=47)
+    q = x["q"].cuda()
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o_c, l_c = fa.forward_decode(q, x["k"].cuda(), x["v"].cuda(), cl, causal=causal, num_splits=num_splits)
+    o_p, l_p = fa.forward_decode_paged(q, kp.cuda(), vp.cuda(), table.cuda(), cl, causal=causal,
+                                       num_splits=num_splits)
+    fa.check_device_error()
+    assert torch.equal(o_c, o_p) and torch.equal(l_c, l_p)
+    xo = {n: f64(x[n]) for n in ("q", "k", "v")}
+    o = f64(o_p.cpu())
+    for b in range(B):
+        ro, _ = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], causal, 1 / math.sqrt(d))
+        assert_close(f"o[b={b}]", o[b], ro, ATOL["bf16"])
+
+
+def test_paged_page_out_of_range_is_reported(fa_lib):
+    fa = fa_lib
+    x = make_decode_inputs(1, 1, 256, 4, 4, 64, dtype="bf16", seed=48)
+    kp, vp, table = _paged(x, 1, 256, [256], seed=49)
+    table[0, 1] = 10_000  # no such page
+    fa.forward_decode_paged(x["q"].cuda(), kp.cuda(), vp.cuda(), table.cuda(),
+                            torch.tensor([256], dtype=torch.int32, device="cuda"), num_splits=1)
+    with pytest.raises(fa.FaError) as e:
+        fa.check_device_error()
+    assert e.value.status == fa.FA_ERR_INVALID
