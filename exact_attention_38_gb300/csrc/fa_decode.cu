@@ -97,6 +97,11 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // The split combine (launched as a programmatic dependent when there are several
+  // splits) may be scheduled once every CTA of this grid is running; it still waits for
+  // the whole grid to finish before it reads a partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- work decode: CTA = (batch, kv head, split); splits of one (b, kv head) are
   // consecutive CTAs
   const int s = static_cast<int>(blockIdx.x % p.S);
@@ -439,47 +444,117 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
 
 // Merges the splits of every packed row: lse = ln sum_s e^{lse_s},
 // O = sum_s e^{lse_s - lse} O_s (a split that saw no key has lse_s = -inf, weight 0).
-// One warp per row, lanes over the row's d/4 float4 columns.
+// Four warps share a row (two rows per CTA): each takes the row's lse from all splits
+// (lanes over splits, a running maximum and rescaled sum per lane, then combined across
+// the warp), adds the partial rows of its own splits s = q, q + 4, ... (lane owns D/32
+// columns; eight row loads in flight), and the four sums meet in shared memory.  With
+// few rows this spreads a row's reads over four warps.  Launched as a programmatic
+// dependent of fa_decode_kernel: griddepcontrol.wait returns once that grid has
+// finished and its writes are visible, so the launch itself overlaps its tail.
+constexpr int kCombWarpsPerRow = 4;
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_decode_combine(const __grid_constant__ DecParams p) {
-  constexpr int LANES = D / 4;
+  constexpr int V = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int WPR = kCombWarpsPerRow, RPC = 8 / WPR;
+  constexpr unsigned FULL = 0xffffffffu;
+  __shared__ float red[8][D];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp % WPR, slot = warp / WPR;
   const long long rows = static_cast<long long>(p.B) * p.Hkv * p.M;
-  const long long warps = static_cast<long long>(gridDim.x) * 8;
-  const int lane = threadIdx.x & 31;
-  for (long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5); w < rows; w += warps) {
-    const int r = static_cast<int>(w % p.M);
-    const long long bh = w / p.M;
-    const int hkv = static_cast<int>(bh % p.Hkv), b = static_cast<int>(bh / p.Hkv);
-    const long long base = bh * p.S * p.M + r;  // partial row of split s: base + s*M
-    float mx = -INFINITY;
-    for (int s = 0; s < p.S; ++s) mx = fmaxf(mx, p.lpart[base + static_cast<long long>(s) * p.M]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int nmine = (p.S - q + WPR - 1) / WPR;  // splits q, q + WPR, ... of this warp
+  for (long long r0 = static_cast<long long>(blockIdx.x) * RPC; r0 < rows;
+       r0 += static_cast<long long>(gridDim.x) * RPC) {  // uniform over the CTA
+    const long long w = r0 + slot;
+    const bool valid = w < rows;
+    float acc[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[c] = 0.f;
     float lse = -INFINITY;
-    if (mx != -INFINITY) {
-      float tot = 0.f;
-      for (int s = 0; s < p.S; ++s) tot += expf(p.lpart[base + static_cast<long long>(s) * p.M] - mx);
-      lse = mx + logf(tot);
-      for (int s = 0; s < p.S; ++s) {
-        const long long prow = base + static_cast<long long>(s) * p.M;
-        const float wgt = expf(p.lpart[prow] - lse);
-        if (lane < LANES && wgt > 0.f) {
-          const float4 v = reinterpret_cast<const float4*>(p.opart + prow * D)[lane];
-          acc[0] += wgt * v.x;
-          acc[1] += wgt * v.y;
-          acc[2] += wgt * v.z;
-          acc[3] += wgt * v.w;
+    int r = 0, hkv = 0, b = 0;
+    if (valid) {  // uniform over the warp
+      r = static_cast<int>(w % p.M);
+      const long long bh = w / p.M;
+      hkv = static_cast<int>(bh % p.Hkv);
+      b = static_cast<int>(bh / p.Hkv);
+      const long long base = bh * p.S * p.M + r;  // partial row of split s: base + s*M
+      const float* lp = p.lpart + base;
+      float m = -INFINITY, t = 0.f;
+      for (int s = lane; s < p.S; s += 32) {
+        const float x = lp[static_cast<long long>(s) * p.M];
+        if (x > m) {
+          t = t * expf(m - x) + 1.f;  // e^{-inf} = 0 on the first finite value
+          m = x;
+        } else if (x != -INFINITY) {
+          t += expf(x - m);
+        }
+      }
+      float mx = m;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+      if (mx != -INFINITY) {
+        float tot = m == -INFINITY ? 0.f : t * expf(m - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        lse = mx + logf(tot);
+        const float* op = p.opart + base * D + lane * V;
+        for (int c0 = 0; c0 < nmine; c0 += 32) {
+          const int mine = c0 + lane;
+          const float wl =
+              mine < nmine ? expf(lp[static_cast<long long>(q + WPR * mine) * p.M] - lse) : 0.f;
+          const int n = min(32, nmine - c0);
+          for (int j0 = 0; j0 < n; j0 += 8) {
+            float v[8][V];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (j0 + u < n) {
+                const float* src = op + static_cast<long long>(q + WPR * (c0 + j0 + u)) * p.M * D;
+                if constexpr (V == 4) {
+                  const float4 x4 = *reinterpret_cast<const float4*>(src);
+                  v[u][0] = x4.x, v[u][1] = x4.y, v[u][2] = x4.z, v[u][3] = x4.w;
+                } else {
+                  const float2 x2 = *reinterpret_cast<const float2*>(src);
+                  v[u][0] = x2.x, v[u][1] = x2.y;
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < V; ++c) v[u][c] = 0.f;
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float wj = __shfl_sync(FULL, wl, (j0 + u) & 31);
+              if (j0 + u < n && wj > 0.f) {
+#pragma unroll
+                for (int c = 0; c < V; ++c) acc[c] = fmaf(wj, v[u][c], acc[c]);
+              }
+            }
+          }
         }
       }
     }
-    const int i = r / p.G, h = hkv * p.G + r % p.G;
-    if (lane < LANES) {
-      uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D;
-      uint2 o2;
-      o2.x = dec_pack2<BF16>(acc[0], acc[1]);
-      o2.y = dec_pack2<BF16>(acc[2], acc[3]);
-      reinterpret_cast<uint2*>(orow)[lane] = o2;
+#pragma unroll
+    for (int c = 0; c < V; ++c) red[warp][lane * V + c] = acc[c];
+    __syncthreads();
+    if (valid && q == 0) {
+#pragma unroll
+      for (int k = 1; k < WPR; ++k)
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[c] += red[warp + k][lane * V + c];
+      const int i = r / p.G, h = hkv * p.G + r % p.G;
+      uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D + lane * V;
+      if constexpr (V == 4) {
+        uint2 o2;
+        o2.x = dec_pack2<BF16>(acc[0], acc[1]);
+        o2.y = dec_pack2<BF16>(acc[2], acc[3]);
+        *reinterpret_cast<uint2*>(orow) = o2;
+      } else {
+        *reinterpret_cast<uint32_t*>(orow) = dec_pack2<BF16>(acc[0], acc[1]);
+      }
+      if (lane == 0) p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = lse;
     }
-    if (lane == 0) p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = lse;
+    __syncthreads();
   }
 }
 
@@ -494,9 +569,18 @@ static cudaError_t launch_decode_t(const DecParams& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess || p.S == 1) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hkv * p.M;
-  const long long blocks = (rows + 7) / 8;
-  fa_decode_combine<D, BF16><<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  const long long blocks = (rows + 8 / kCombWarpsPerRow - 1) / (8 / kCombWarpsPerRow);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks < 4096 ? blocks : 4096));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_decode_combine<D, BF16>, p);
 }
 
 cudaError_t launch_decode(const DecParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {

@@ -81,3 +81,52 @@ def test_cuda_graph_capture_and_replay(fa_lib):
         fa.check_device_error()
         for r, t in zip(ref, (o, lse, dq, dk, dv)):
             assert torch.equal(r, t)
+
+
+def _decode_inputs(seed):
+    from exact_attention_38_gb300.inputs import make_decode_inputs
+
+    x = make_decode_inputs(2, 1, 3000, 16, 2, 128, dtype="bf16", seed=seed)
+    return x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
+
+
+def test_decode_split_combine_in_graph_and_back_to_back(fa_lib):
+    """The split combine is launched as a programmatic dependent of the decode kernel:
+    back-to-back calls that reuse one workspace, and a captured graph replayed with new
+    cache lengths, give the bits of separate eager calls."""
+    fa = fa_lib
+    q, k, v = _decode_inputs(603)
+    lens_list = [[3000, 1], [129, 2999], [1500, 1500]]
+    refs = []
+    for lens in lens_list:
+        cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        o, lse = fa.forward_decode(q, k, v, cl, num_splits=6)
+        torch.cuda.synchronize()
+        refs.append((o.clone(), lse.clone()))
+    ws = torch.empty(fa.fa_decode_workspace_size(2, 16, 2, 1, 3000, 128, 6), dtype=torch.uint8, device="cuda")
+    o, lse = torch.empty_like(q), torch.empty((2, 16, 1), dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(2):  # back to back on one stream, one workspace
+        for lens in lens_list:
+            cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+            fa.forward_decode(q, k, v, cl, num_splits=6, out=o, lse=lse, workspace=ws)
+            outs.append((o.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    fa.check_device_error()
+    for n, (og, lg) in enumerate(outs):
+        assert torch.equal(og, refs[n % 3][0]) and torch.equal(lg, refs[n % 3][1])
+    cl = torch.tensor(lens_list[0], dtype=torch.int32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fa.forward_decode(q, k, v, cl, num_splits=6, out=o, lse=lse, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    for n, lens in enumerate(lens_list):
+        cl.copy_(torch.tensor(lens, dtype=torch.int32))
+        o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        fa.check_device_error()
+        assert torch.equal(o, refs[n][0]) and torch.equal(lse, refs[n][1])
