@@ -2,11 +2,13 @@
 
 Tolerance, derived from the arithmetic (the pages and the problem statement fix none for
 8-bit inputs): the scores are exact products of the stored values accumulated in fp32,
-so lse is held to the usual 1e-3.  P is rounded to E4M3 as P * 2^8 before the P V
+so lse is held to the usual 1e-3.  P is rounded to E4M3 as P * 2^7 before the P V
 product: a relative error of at most 2^-4 per term (3 mantissa bits, round to nearest),
-or an absolute 2^-18 where P * 2^8 falls in E4M3's subnormal range; the bf16 output adds
-2^-9 relative.  So element (i, c) of O may differ by at most
-    2^-4 * sum_j P_ij |v_jc| + 2^-18 * sum_j |v_jc| + 2^-8 |O_ic| (+ 1e-5 for fp32 sums),
+or an absolute 2^-17 where P * 2^7 falls in E4M3's subnormal range (half the 2^-9
+subnormal step, divided by the 2^7; the kernel's row sum l >= 1, so the bound holds
+for the normalised P); the bf16 output adds 2^-9 relative.  So element (i, c) of O may
+differ by at most
+    2^-4 * sum_j P_ij |v_jc| + 2^-17 * sum_j |v_jc| + 2^-8 |O_ic| (+ 1e-5 for fp32 sums),
 computed per element from the oracle's P.  The relative-norm error is also reported
 against a loose 2^-4 (every term at its worst)."""
 
@@ -55,7 +57,7 @@ def _check(fa, B, N, Hq, Hkv, causal, seed, rows=None, heads=None):
             assert np.max(np.abs(lse[b, h, rows] - rl)) <= 1e-3
             p = _p_rows(q, k, causal, scale, b, h, rows, rl)
             av = np.abs(v[b, :, h // g, :])
-            tol = 2.0 ** -4 * (p @ av) + 2.0 ** -18 * av.sum(axis=0)[None, :] + 2.0 ** -8 * np.abs(ro) + 1e-5
+            tol = 2.0 ** -4 * (p @ av) + 2.0 ** -17 * av.sum(axis=0)[None, :] + 2.0 ** -8 * np.abs(ro) + 1e-5
             got = o[b, rows, h, :]
             assert np.all(np.isfinite(got))
             bad = np.abs(got - ro) > tol
