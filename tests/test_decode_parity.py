@@ -131,3 +131,27 @@ def test_paged_page_out_of_range_is_reported(fa_lib):
     with pytest.raises(fa.FaError) as e:
         fa.check_device_error()
     assert e.value.status == fa.FA_ERR_INVALID
+
+
+@pytest.mark.parametrize("dtype,d,Nq,G", [("fp16", 64, 4, 4), ("bf16", 64, 1, 8), ("fp16", 128, 3, 2)])
+def test_paged_cache_other_shapes(fa_lib, dtype, d, Nq, G):
+    """Paged caches with d = 64, fp16 and several queries under the bottom-right mask:
+    the same bits as the contiguous cache, within tolerance of the oracle, lse included."""
+    fa = fa_lib
+    B, Nmax, Hkv = 2, 700, 2
+    Hq = G * Hkv
+    lens = [700, 257]
+    x = make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype=dtype, seed=50 + d + Nq)
+    kp, vp, table = _paged(x, B, Nmax, lens, seed=51)
+    q = x["q"].cuda()
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o_c, l_c = fa.forward_decode(q, x["k"].cuda(), x["v"].cuda(), cl, causal=True, num_splits=3)
+    o_p, l_p = fa.forward_decode_paged(q, kp.cuda(), vp.cuda(), table.cuda(), cl, causal=True, num_splits=3)
+    fa.check_device_error()
+    assert torch.equal(o_c, o_p) and torch.equal(l_c, l_p)
+    xo = {n: f64(x[n]) for n in ("q", "k", "v")}
+    o, lse = f64(o_p.cpu()), l_p.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        ro, rl = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], True, 1 / math.sqrt(d))
+        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype])
+        assert np.max(np.abs(lse[b] - rl)) <= LSE_ATOL
