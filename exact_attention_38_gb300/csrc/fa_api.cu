@@ -1,6 +1,7 @@
 // C ABI of libfa.so: argument validation, tensor-map encoding, launches.
 // Every argument check happens before the first CUDA call, so a bad call returns
 // an error code without touching the device (and works on a host without a GPU).
+#include "fa_decode_policy.h"
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -77,16 +78,17 @@ fa_status check_varlen(int B, int Hq, int Hkv, int total_q, int total_k, int max
 bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Split count of the decode pass: as many splits as fit one wave of CTA slots on a
-// 152-SM part at two CTAs per SM (304; a fixed target, so the workspace size does not
-// depend on the device; measured best on GB300 against 2-4x more CTAs), never more
-// splits than key blocks; `want` > 0 overrides the target.
+// 152-SM part (304 at two CTAs per SM, or 152 with the deep K/V ring of
+// decode_deep_ring; a fixed target, so the workspace size does not depend on the
+// device; measured best on GB300 against 2-4x more CTAs), never more splits than key
+// blocks; `want` > 0 overrides the target.
 struct DecodeSplit {
   int S, cps;
 };
-DecodeSplit decode_split(int B, int Hkv, int Nmax, int want) {
+DecodeSplit decode_split(int B, int Hkv, int Nmax, int d, int want) {
   const int nkb = (Nmax + 127) / 128;
   const long long units = static_cast<long long>(B) * Hkv;
-  long long S = want > 0 ? want : 304 / units;
+  long long S = want > 0 ? want : decode_cta_slots(d, units) / units;
   if (S > nkb) S = nkb;
   if (S < 1) S = 1;
   const int cps = static_cast<int>((nkb + S - 1) / S);
@@ -103,7 +105,7 @@ fa_status check_decode(int B, int Hq, int Hkv, int Nq, int Nmax, int d, float sc
   if (Nmax > (1 << 24)) return FA_ERR_UNSUPPORTED;
   const long long kv = static_cast<long long>(B) * Nmax * Hkv * d * 2;
   if (kv >= (1LL << 40) || static_cast<long long>(B) * Nq * Hq * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hkv * decode_split(B, Hkv, Nmax, num_splits).S >= (1LL << 31))
+  if (static_cast<long long>(B) * Hkv * decode_split(B, Hkv, Nmax, d, num_splits).S >= (1LL << 31))
     return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -113,7 +115,7 @@ struct DecodeWorkspace {
 };
 DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, d, num_splits);
   DecodeWorkspace w{};
   if (sp.S == 1) return w;
   const size_t rows = static_cast<size_t>(B) * Hkv * sp.S * (Hq / Hkv) * Nq;
@@ -452,7 +454,7 @@ size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nmax, int d,
 
 int fa_decode_num_splits(int B, int Hq, int Hkv, int Nq, int Nmax, int d, int num_splits) {
   if (check_decode(B, Hq, Hkv, Nq, Nmax, d, 1.0f, FA_BF16, num_splits) != FA_OK) return 0;
-  return decode_split(B, Hkv, Nmax, num_splits).S;
+  return decode_split(B, Hkv, Nmax, d, num_splits).S;
 }
 
 fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache, const int* cache_seqlens, void* o,
@@ -464,7 +466,7 @@ fa_status fa_fwd_decode(const void* q, const void* k_cache, const void* v_cache,
   if (!aligned4(cache_seqlens)) return FA_ERR_INVALID;
   const fa_status st = check_decode(B, Hq, Hkv, Nq, Nmax, d, scale, static_cast<int>(dtype), num_splits);
   if (st != FA_OK) return st;
-  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, d, num_splits);
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, Nq, Nmax, d, num_splits);
   if (ws.total > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                        workspace_bytes < ws.total))
@@ -553,7 +555,7 @@ fa_status fa_fwd_decode_paged(const void* q, const void* k_pages, const void* v_
   const fa_status st = check_decode(B, Hq, Hkv, Nq, Nmax, d, scale, static_cast<int>(dtype), num_splits);
   if (st != FA_OK) return st;
   if (static_cast<long long>(num_pages) * 128 * Hkv * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
-  const DecodeSplit sp = decode_split(B, Hkv, Nmax, num_splits);
+  const DecodeSplit sp = decode_split(B, Hkv, Nmax, d, num_splits);
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, Nq, Nmax, d, num_splits);
   if (ws.total > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                        workspace_bytes < ws.total))

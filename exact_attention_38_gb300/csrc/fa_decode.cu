@@ -21,7 +21,10 @@
 //  * two CTAs per SM (256 threads, 256 TMEM columns and < 100 KB shared memory each),
 //    so the two CTAs' K/V streams overlap each other's serial softmax / MMA chain
 //    (the softmax warpgroup runs with 176 registers, the control warps with 80);
-//    the pass is bound by the HBM bytes of the cache.
+//    the pass is bound by the HBM bytes of the cache.  With at most 8 (batch, kv head)
+//    units at d = 128 a deeper K/V ring at one CTA per SM is used instead (the rule
+//    and its measurements are in fa_decode_policy.h).
+#include "fa_decode_policy.h"
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -30,17 +33,18 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool DEEP>
 struct DecCfg {
   static constexpr int CHUNKS = D / 64;
   static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile, or one K / V block of 128 keys
   static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  // K/V ring: one block (K and V) in flight at two CTAs per SM, two with the deep ring
+  static constexpr int STAGES = (D == 128 && !DEEP) ? 2 : 4;
   static constexpr int THREADS = 256;             // softmax warpgroup + control warpgroup
   static constexpr int NBARS = 4 + 2 * STAGES + 1;
   static constexpr int SMEM = 1024 + (1 + STAGES) * TILE_BYTES + 8 * NBARS + 64;
   static constexpr uint32_t TMEM_COLS = 256;      // S (128) and O (D <= 128)
-  static_assert(2 * SMEM <= 232448, "two CTAs per SM");
+  static_assert((DEEP ? 1 : 2) * SMEM <= 232448, "CTAs per SM");
 };
 
 __device__ __forceinline__ float dec_ex2(float x) {
@@ -76,9 +80,9 @@ __device__ __forceinline__ void dec_write_empty_row(const DecParams& p, int b, i
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DEEP>
 __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant__ DecParams p) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, DEEP>;
   extern __shared__ uint8_t smem_raw_dec[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_dec) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -558,10 +562,10 @@ __global__ void __launch_bounds__(256) fa_decode_combine(const __grid_constant__
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DEEP = false>
 static cudaError_t launch_decode_t(const DecParams& p, cudaStream_t stream) {
-  using C = DecCfg<D>;
-  auto kern = fa_decode_kernel<D, BF16, CAUSAL>;
+  using C = DecCfg<D, DEEP>;
+  auto kern = fa_decode_kernel<D, BF16, CAUSAL, DEEP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.B) * p.Hkv * p.S;
@@ -585,6 +589,11 @@ static cudaError_t launch_decode_t(const DecParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream) {
   const bool bf = dtype == FA_BF16;
+  if (d == 128 && decode_deep_ring(d, static_cast<long long>(p.B) * p.Hkv)) {
+    if (bf)
+      return causal ? launch_decode_t<128, true, true, true>(p, stream) : launch_decode_t<128, true, false, true>(p, stream);
+    return causal ? launch_decode_t<128, false, true, true>(p, stream) : launch_decode_t<128, false, false, true>(p, stream);
+  }
   if (d == 128) {
     if (bf) return causal ? launch_decode_t<128, true, true>(p, stream) : launch_decode_t<128, true, false>(p, stream);
     return causal ? launch_decode_t<128, false, true>(p, stream) : launch_decode_t<128, false, false>(p, stream);

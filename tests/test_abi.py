@@ -223,6 +223,25 @@ def test_decode_paged_argument_errors_need_no_device(lib, kw, code):
     assert _decode_paged(lib, **kw) == code
 
 
+def test_decode_split_targets_one_wave(lib):
+    """Automatic split count: one wave of CTAs on 152 SMs, 304 slots at two CTAs per SM,
+    or 152 when the deep K/V ring (one CTA per SM) is used, i.e. at d = 128 with at most
+    8 (batch, kv head) units; never more splits than 128-key blocks.  Splits take equal
+    block counts, cps = ceil(blocks / target), so the count is ceil(blocks / cps)."""
+    i = ctypes.c_int
+    lib.fa_decode_num_splits.restype = i
+    lib.fa_decode_num_splits.argtypes = [i] * 7
+    n = lambda B, Hkv, N, d: lib.fa_decode_num_splits(B, 4 * Hkv, Hkv, 1, N, d, 0)
+    assert n(1, 8, 65536, 128) == 19  # deep ring: 8 units x 19 = 152 CTAs
+    assert n(2, 4, 65536, 128) == 19
+    assert n(2, 8, 65536, 128) == 19  # 16 units: 304 // 16
+    assert n(4, 8, 65536, 128) == 9
+    assert n(1, 8, 65536, 64) == 37  # d = 64 keeps two CTAs per SM: target 38, 14 blocks each
+    assert n(1, 1, 65536, 128) == 128  # target 152: 4 of the 512 blocks each
+    assert n(1, 8, 1000, 128) == 8  # capped by the 8 key blocks
+    assert n(64, 8, 65536, 128) == 1
+
+
 def test_decode_split_count_and_workspace(lib):
     i = ctypes.c_int
     lib.fa_decode_num_splits.restype = i

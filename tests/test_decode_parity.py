@@ -62,6 +62,13 @@ def test_long_cache_many_splits(fa_lib):
     _check(fa_lib, 1, 2, 40000, 32, 8, 128, [39999], "bf16", True, 0, 44)
 
 
+@pytest.mark.parametrize("causal,Nq,num_splits", [(False, 1, 0), (True, 3, 0), (True, 1, 4), (False, 2, 1)])
+def test_two_ctas_per_sm_shape(fa_lib, causal, Nq, num_splits):
+    # 6 x 2 = 12 (batch, kv head) units at d = 128: the two-CTAs-per-SM ring (at most 8
+    # units take the deep ring, which the tests above cover)
+    _check(fa_lib, 6, Nq, 1700, 8, 2, 128, [1700, 1, 129, 0, 900, 1313], "bf16", causal, num_splits, 52)
+
+
 def test_length_out_of_range_is_reported(fa_lib):
     fa = fa_lib
     x = make_decode_inputs(2, 1, 256, 4, 4, 64, dtype="bf16", seed=45)
