@@ -165,3 +165,25 @@ def test_planted_top_left_mask_is_caught(monkeypatch):
     monkeypatch.setattr(ov, "visible", top_left)
     with pytest.raises(AssertionError):
         test_single_query_sees_every_key_under_the_mask()
+
+
+@pytest.mark.parametrize("cuts", [(0, 5, 13), (0, 1, 2, 3, 13), (0, 13), (0, 0, 7, 7, 13)])
+def test_split_keys_merge_by_lse_weights(cuts):
+    """Splitting the keys into consecutive ranges and merging the per-range results with
+    lse = ln sum_s e^{lse_s} and O = sum_s e^{lse_s - lse} O_s gives attention over all
+    keys: the identity split-key decoding relies on.  Empty ranges carry lse = -inf and
+    weight 0.  Checked against the whole-range oracle and scalar brute force."""
+    q, k, v, _ = _seq(3, 13, 4, 2, 5, seed=21)
+    scale = 0.45
+    parts = [oracle.attn_fwd_qk(q, k[a:b], v[a:b], False, scale) for a, b in zip(cuts[:-1], cuts[1:])]
+    lses = np.stack([pl for _, pl in parts])  # [S, Hq, Nq]
+    mx = np.max(lses, axis=0)
+    lse = mx + np.log(np.sum(np.exp(lses - mx), axis=0))
+    w = np.exp(lses - lse)  # [S, Hq, Nq]
+    o = sum(np.transpose(w[s_], (1, 0))[:, :, None] * parts[s_][0] for s_ in range(len(parts)))
+    ro, rl = oracle.attn_fwd_qk(q, k, v, False, scale)
+    np.testing.assert_allclose(lse, rl, atol=1e-12)
+    np.testing.assert_allclose(o, ro, atol=1e-12)
+    bo, bl = oracle.brute_force_fwd_qk(q, k, v, False, scale)
+    np.testing.assert_allclose(o, bo, atol=1e-12)
+    np.testing.assert_allclose(lse, bl, atol=1e-12)
