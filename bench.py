@@ -141,6 +141,36 @@ def job_throughput(flops_per_rank_step, world, ms_step):
     return world * flops_per_rank_step / (ms_step * 1e-3) / 1e12
 
 
+# ------------------------------------------------------------- host cost per call
+
+def host_us_per_call(fn, reps=50):
+    """Median host time of one call (argument checks, tensor-map encoding, launches),
+    measured with the GPU idle: the device is synchronised before every call, and the
+    call returns once its kernels are enqueued.  Includes the Python-to-C (ctypes)
+    marshalling of the call."""
+    import torch
+
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    return statistics.median(ts) * 1e6
+
+
+def ctypes_floor_us(fa, reps=200):
+    """Median time of a call into the library that does nothing (fa_status_string): the
+    marshalling part of the per-call figures."""
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fa.lib.fa_status_string(0)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts) * 1e6
+
+
 # ----------------------------------------------------------- clocks during timing
 
 class ClockSampler:
@@ -347,6 +377,9 @@ def run_native(a):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     fa.check_device_error()
+    host_us = {"fa_fwd": host_us_per_call(fwd), bwd_fn.__name__: host_us_per_call(bwd),
+               "ctypes_floor": ctypes_floor_us(fa),
+               "how": "median over 50 calls, GPU idle (synchronised before each call), ctypes marshalling included"}
     per = {n: [e0.elapsed_time(e1) for e0, e1 in ev[n]] for n in ev}
     ms_step = reduce_step_time(sum(statistics.mean(per[n]) for n in per), world, dev)
     if world > 1:
@@ -462,7 +495,7 @@ def run_native(a):
                        "l2": "flushed between steps (2x L2 buffer written outside the timed events); "
                              "inputs (q,k,v,dO,o = 320 MiB) also exceed L2"},
             "passes": passes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * K, "wall_s_timed_region": t_wall,
+            "gpu_launches": launches_per_step * K, "wall_s_timed_region": t_wall, "host_us_per_call": host_us,
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -652,6 +685,9 @@ def run_decode(a):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
     fa.check_device_error()
+    host_us = {"fa_fwd_decode_paged" if a.paged else "fa_fwd_decode": host_us_per_call(step),
+               "ctypes_floor": ctypes_floor_us(fa),
+               "how": "median over 50 calls, GPU idle (synchronised before each call), ctypes marshalling included"}
     ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     # algorithmic bytes: every cached key and value row once, q read, o and lse written
     kv_bytes = 2 * B * N * Hkv * d * 2
@@ -673,7 +709,7 @@ def run_decode(a):
                          "peak": peak_hbm, "unit": "GB/s", "frac": gbs / peak_hbm, "traffic": None,
                          "bytes_per_step": kv_bytes + io_bytes, "peak_kind": f"{peak_kind} HBM copy (of measured)"},
             "cpu_baseline": None, "e2e": None, "gpu_launches": (2 if S > 1 else 1) * a.steps,
-            "clocks": clk.summary()}
+            "host_us_per_call": host_us, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 

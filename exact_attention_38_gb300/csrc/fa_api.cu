@@ -150,6 +150,20 @@ unsigned* device_error_word() {
   return p;
 }
 
+int device_sm_count() {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_acquire);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 148;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(sms, std::memory_order_release);
+  return sms;
+}
+
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
                      fa_dtype dtype) {
   return encode_bshd_box_map(map, base, B, N, H, d, 1, box_rows, dtype);

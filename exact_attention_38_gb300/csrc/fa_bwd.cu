@@ -800,9 +800,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
 template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   {
     // preprocess: LPR lanes per row, 8 rows per 256-thread block and step
     const long long rows = VARLEN ? static_cast<long long>(p.B) * p.Hq * p.Npad : static_cast<long long>(p.B) * p.N * p.Hq;
@@ -817,7 +815,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   }
   {
     auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = set_smem_limit_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM);
     if (e != cudaSuccess) return e;
     const long long nk = VARLEN ? p.vl.max_k : p.N;
     const long long grid = ((nk + 127) / 128) * p.B * p.Hkv;

@@ -477,7 +477,7 @@ template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_limit_once<fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>>(C::SMEM);
   if (e != cudaSuccess) return e;
   const long long nqb = ((VARLEN ? p.vl.max_q : p.N) + 255) / 256;
   const long long grid = nqb * p.B * p.Hq;

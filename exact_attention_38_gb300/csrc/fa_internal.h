@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -128,6 +129,25 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d);
 bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, int d);
 
 unsigned* device_error_word();  // address of this device's error word (device memory)
+
+// Raises kernel `Kern`'s dynamic shared-memory limit to `bytes`, once per device: the
+// attribute belongs to the function on the current device and stays set, so repeating
+// it on every launch only costs host time.  (Devices 64 and up repeat it every call.)
+template <auto Kern>
+cudaError_t set_smem_limit_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Streaming-multiprocessor count of the current device (looked up once per device).
+int device_sm_count();
 
 cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
 // deterministic: dK/dV from the key-block kernel without its dQ path, then dQ from the

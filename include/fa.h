@@ -35,8 +35,18 @@
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  Argument errors are reported synchronously, before any
  *    work is enqueued.  Errors inside a kernel (a bounded wait that ran out) are
- *    recorded in a per-device error word that fa_check_device_error() reads.
- *  - Calls on different streams may overlap; the library keeps no per-call state.
+ *    recorded in a per-device error word that fa_check_device_error() reads.  That
+ *    word is shared by every stream and host thread using the device: a check on one
+ *    stream reports, and clears, an error raised by a kernel on any stream of the
+ *    device, including one that has not finished when the check reads the word.
+ *  - Calls on different streams may overlap; the library keeps no per-call state,
+ *    except fa_bwd_noalloc, whose calls all share one scratch array and must be
+ *    serialised (see there).
+ *  - Per device the library remembers a few addresses and settings (the error word's
+ *    and fa_bwd_noalloc's scratch addresses, each kernel's shared-memory limit), taken
+ *    on the first call that needs them.  cudaDeviceReset() discards them on the device
+ *    side, so the library must not be used on a device after cudaDeviceReset() in the
+ *    same process.
  *  - The compute entry points may be captured into a CUDA graph and replayed (their
  *    host-side work, tensor-map encoding and launch attributes, happens at capture and
  *    is baked into the graph's kernel parameters; the buffers must then stay at the
@@ -254,7 +264,7 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
  *   tensor's descale (q_descale, k_descale, v_descale: finite, > 0).
  *   o [B,N,Hq,128]: bf16.  lse [B,Hq,N]: fp32, natural log of the scaled scores.
  * Scores and their softmax are computed in fp32 from the 8-bit products; P is rounded to
- * E4M3 (as P * 2^8) for the P V product, so O carries up to 2^-4 relative error per term
+ * E4M3 (as P * 2^7) for the P V product, so O carries up to 2^-4 relative error per term
  * of its sum over keys.  Head dimension 128 only (FA_ERR_UNSUPPORTED otherwise).
  * workspace: at least fa_fwd_fp8_workspace_size() bytes, 256-byte aligned; it receives a
  * transposed copy of V (the 8-bit P V product reads V with keys contiguous).

@@ -29,3 +29,22 @@ def fa_lib():
     from exact_attention_38_gb300 import fa
 
     return fa
+
+
+def pytest_terminal_summary(terminalreporter):
+    """How many compared elements exceeded the flat max-abs figure (the bound the tests
+    apply adds half a unit in the last place of the output format at the reference)."""
+    try:
+        from _parity import FLAT_EXCESS
+    except ImportError:
+        return
+    if not FLAT_EXCESS:
+        return
+    n = sum(c for _, c, _, _ in FLAT_EXCESS)
+    tot = sum(t for _, _, t, _ in FLAT_EXCESS)
+    terminalreporter.write_line(
+        f"parity: {n} of {tot} elements in {len(FLAT_EXCESS)} comparisons exceeded the flat max-abs figure "
+        f"(all within it plus half an output ulp); largest |ref| among them "
+        f"{max(r for _, _, _, r in FLAT_EXCESS):.3f}")
+    for name, c, t, r in sorted(FLAT_EXCESS, key=lambda e: -e[1])[:10]:
+        terminalreporter.write_line(f"  {name}: {c} of {t} (max |ref| {r:.3f})")

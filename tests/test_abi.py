@@ -279,3 +279,22 @@ def test_fp8_argument_errors_need_no_device(lib):
         a = list(base)
         a[idx] = val
         assert fn(*a) == code, (idx, val)
+
+
+def test_noalloc_scratch_limit_needs_no_device(lib):
+    """fa_bwd_noalloc's fixed scratch: with B=1, Hq=16, d=128 the backward workspace fits
+    up to N=4032 (Npad 4032) and not at N=4033 (Npad 4096); there the call is rejected
+    with FA_ERR_UNSUPPORTED before any CUDA call, so it answers on a host without a GPU."""
+    m = re.search(r"#define\s+FA_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", open(HEADER).read())
+    limit = int(m.group(1)) << int(m.group(2))
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 5
+    assert lib.fa_bwd_workspace_size(1, 16, 16, 4032, 128) <= limit
+    assert lib.fa_bwd_workspace_size(1, 16, 16, 4033, 128) > limit
+    f = lib.fa_bwd_noalloc
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp] * 9 + [i] * 6 + [ctypes.c_float, i, vp]
+    f.restype = i
+    fake = 1 << 20
+    assert f(*([fake] * 9), 1, 16, 16, 4033, 128, 0, 0.088, 0, None) == 2
+    assert f(*([fake] * 9), 1, 16, 16, 8192, 128, 1, 0.088, 1, None) == 2

@@ -31,7 +31,7 @@ def _check(fa, B, Nq, Nmax, Hq, Hkv, d, lens, dtype, causal, num_splits, seed):
     xo = {n: f64(x[n]) for n in ("q", "k", "v")}
     for b in range(B):
         ro, rl = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], causal, scale)
-        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype])
+        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype], dtype)
         assert np.array_equal(np.isneginf(lse[b]), np.isneginf(rl)), f"lse[b={b}]: rows without keys must be -inf"
         fin = np.isfinite(rl)
         if fin.any():
@@ -125,7 +125,7 @@ def test_paged_cache_matches_contiguous(fa_lib, causal, num_splits):
     o = f64(o_p.cpu())
     for b in range(B):
         ro, _ = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], causal, 1 / math.sqrt(d))
-        assert_close(f"o[b={b}]", o[b], ro, ATOL["bf16"])
+        assert_close(f"o[b={b}]", o[b], ro, ATOL["bf16"], "bf16")
 
 
 def test_paged_page_out_of_range_is_reported(fa_lib):
@@ -160,5 +160,5 @@ def test_paged_cache_other_shapes(fa_lib, dtype, d, Nq, G):
     o, lse = f64(o_p.cpu()), l_p.cpu().numpy().astype(np.float64)
     for b in range(B):
         ro, rl = oracle.attn_fwd_qk(xo["q"][b], xo["k"][b, :lens[b]], xo["v"][b, :lens[b]], True, 1 / math.sqrt(d))
-        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype])
+        assert_close(f"o[b={b}]", o[b], ro, ATOL[dtype], dtype)
         assert np.max(np.abs(lse[b] - rl)) <= LSE_ATOL

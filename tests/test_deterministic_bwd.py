@@ -32,7 +32,7 @@ def test_parity_ragged(fa_lib, N, causal, d):
     xo = {n: f64(t) for n, t in x.items()}
     ref = oracle.attn_bwd_ref(xo["q"], xo["k"], xo["v"], xo["do"], causal, 1.0 / math.sqrt(d))
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
-        assert_close(name, f64(got.cpu()), ref[name], ATOL["bf16"])
+        assert_close(name, f64(got.cpu()), ref[name], ATOL["bf16"], "bf16")
         assert_relnorm(name, f64(got.cpu()), ref[name])
 
 
@@ -44,7 +44,7 @@ def test_parity_gqa(fa_lib, dtype, causal):
     xo = {n: f64(t) for n, t in x.items()}
     ref = oracle.attn_bwd_ref(xo["q"], xo["k"], xo["v"], xo["do"], causal, 1.0 / math.sqrt(128))
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
-        assert_close(name, f64(got.cpu()), ref[name], ATOL[dtype])
+        assert_close(name, f64(got.cpu()), ref[name], ATOL[dtype], dtype)
         assert_relnorm(name, f64(got.cpu()), ref[name])
 
 
@@ -71,4 +71,4 @@ def test_bitwise_repeatable_and_dkdv_match(fa_lib, causal):
     for h in (0, 9):
         ref = oracle.attn_bwd_dq_rows(xo["q"], xo["k"], xo["v"], xo["do"], causal, scale, 1, h, rows)
         got = f64(runs[0][0][1, rows, h, :].cpu())
-        assert_close("dq", got, ref, ATOL["bf16"])
+        assert_close("dq", got, ref, ATOL["bf16"], "bf16")

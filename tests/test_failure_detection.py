@@ -40,4 +40,4 @@ def test_bounded_wait_reports_timeout_and_context_survives(fa_lib):
     _, o, _ = gpu_forward(fa, x, True)
     xo = {k: f64(v) for k, v in x.items()}
     want, _ = oracle.attn_fwd_ref(xo["q"], xo["k"], xo["v"], True, 1.0 / math.sqrt(64))
-    assert_close("O", f64(o.cpu()), want, ATOL["bf16"])
+    assert_close("O", f64(o.cpu()), want, ATOL["bf16"], "bf16")

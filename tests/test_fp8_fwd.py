@@ -84,3 +84,13 @@ def test_fp8_benchmark_shape_sampled(fa_lib, causal):
     rng = np.random.default_rng(520)
     rows = np.unique(np.concatenate([rng.choice(4096, 40, replace=False), [0, 4095]]))
     _check(fa_lib, 4, 4096, 16, 16, causal, 521, rows=rows, heads=(0, 11))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_bench_workload_16k_sampled(fa_lib, causal):
+    """The shape and inputs `bench.py --fp8` times: B=1, Hq=Hkv=16, N=16384, seed 3.  At
+    this length each row meets 128 key blocks, so the lazy rescale (threshold 1.5 in log2
+    units) and the 2^7 pre-scale of P are exercised four times longer than at N=4096."""
+    rng = np.random.default_rng(530)
+    rows = np.unique(np.concatenate([rng.choice(16384, 48, replace=False), [0, 16383]]))
+    _check(fa_lib, 1, 16384, 16, 16, causal, 3, rows=rows, heads=(0, 7, 15))

@@ -18,7 +18,7 @@ def _check_full(fa, B, N, Hq, Hkv, d, dtype, causal, seed):
     _, o, lse = gpu_forward(fa, x, causal)
     xo = {k: f64(v) for k, v in x.items()}
     want_o, want_lse = oracle.attn_fwd_ref(xo["q"], xo["k"], xo["v"], causal, 1.0 / math.sqrt(d))
-    assert_close("O", f64(o.cpu()), want_o, ATOL[dtype])
+    assert_close("O", f64(o.cpu()), want_o, ATOL[dtype], dtype)
     assert_close("lse", lse.cpu().double().numpy(), want_lse, LSE_ATOL)
 
 
@@ -64,7 +64,7 @@ def test_q_zero_gives_visible_mean_and_log_count(fa_lib, causal):
     cnt = np.arange(1, N + 1) if causal else np.full(N, N)
     mean = np.cumsum(v, axis=0) / cnt[:, None] if causal else np.broadcast_to(v.mean(axis=0), v.shape)
     for h in range(2):
-        assert_close("O", f64(o.cpu())[0, :, h, :], mean, ATOL["fp16"])
+        assert_close("O", f64(o.cpu())[0, :, h, :], mean, ATOL["fp16"], "fp16")
         assert_close("lse", lse.cpu().double().numpy()[0, h], np.log(cnt), 1e-5)
 
 
@@ -74,7 +74,7 @@ def test_causal_row_zero_is_v0_and_rows_normalise(fa_lib):
     _, o, lse = gpu_forward(fa_lib, x, True)
     q, k, v = (f64(x[n])[0] for n in ("q", "k", "v"))
     og, lg = f64(o.cpu())[0], lse.cpu().double().numpy()[0]
-    assert_close("O row 0", og[0], v[0], ATOL["bf16"])
+    assert_close("O row 0", og[0], v[0], ATOL["bf16"], "bf16")
     # probabilities built from the GPU's lse sum to one on every sampled row
     for h in range(2):
         for i in sample_rows(N, 32, 1):
@@ -94,7 +94,7 @@ def _check_sampled(fa, B, N, Hq, Hkv, d, dtype, causal, seed, heads=2, rows=64):
         for h in rng.choice(Hq, size=min(heads, Hq), replace=False):
             r = sample_rows(N, rows, seed + int(h))
             wo, wl = oracle.attn_fwd_rows(xo["q"], xo["k"], xo["v"], causal, 1.0 / math.sqrt(d), b, int(h), r)
-            assert_close(f"O b{b} h{h}", o[b, r, h], wo, ATOL[dtype])
+            assert_close(f"O b{b} h{h}", o[b, r, h], wo, ATOL[dtype], dtype)
             assert_close(f"lse b{b} h{h}", lse[b, h, r], wl, LSE_ATOL)
 
 

@@ -1,4 +1,5 @@
-"""Concurrency and graph capture: the entry points keep no per-call state, so calls on
+"""Concurrency and graph capture: the entry points keep no per-call state (all but
+fa_bwd_noalloc, whose calls share one scratch array and must be serialised), so calls on
 two streams may overlap, and a forward + backward can be captured into a CUDA graph and
 replayed.  The deterministic backward makes every comparison bit-exact."""
 
