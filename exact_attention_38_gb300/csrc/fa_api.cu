@@ -367,7 +367,8 @@ fa_status bwd_fixed(const void* q, const void* k, const void* v, const void* o, 
   p.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(w + ws.dq_acc_off);
   p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
-  if (!deterministic && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d)) return FA_ERR_CUDA;
+  if (!deterministic && d == 64 && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d))
+    return FA_ERR_CUDA;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -447,7 +448,7 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   p.dq_acc = reinterpret_cast<float*>(w + ws.dq_acc_off);
   p.dvec = reinterpret_cast<float*>(w + ws.dvec_off);
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
-  if (!encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, npad, d)) return FA_ERR_CUDA;
+  if (d == 64 && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, npad, d)) return FA_ERR_CUDA;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

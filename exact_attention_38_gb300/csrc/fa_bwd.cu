@@ -23,11 +23,14 @@
 // columns) turn them into P^T and dS^T, both written back as 16-bit pairs into the S^T
 // columns they read (dS^T also to swizzled shared memory); the tensor cores then accumulate
 // dV += P^T dO and dK += dS^T Q in TMEM for the whole walk (A operands from TMEM) and
-// compute dQ^T = K^T dS^T into the same S^T buffer, which a fourth warpgroup stages in
-// shared memory and adds into the fp32 dQ accumulator with TMA bulk tensor reductions
-// while the next step's S^T / dP^T run.  Taking operands from TMEM matters because the
-// tensor cores read shared-memory operands at 128 B/clk per SM, which otherwise bounds
-// this kernel.
+// compute dQ^T = K^T dS^T into the same S^T buffer, which a fourth warpgroup reads out
+// and adds into the fp32 dQ accumulator while the next step's dP^T / S^T run: at d=128
+// straight from registers (one coalesced reduction per query and warp: 32 consecutive d,
+// 128 bytes); at d=64, where only two of its warps hold dQ^T rows, through a swizzled
+// shared-memory tile and TMA tensor reductions (measured faster there).
+// Taking operands from TMEM, and keeping the dQ^T additions out of shared memory, matters
+// because the tensor cores read shared-memory operands at 128 B/clk per SM and every other
+// shared-memory access competes with them.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -47,7 +50,6 @@ struct BwdCfg {
   static constexpr int Q_CHUNK = 64 * 128;        // 64 rows x 128 B
   static constexpr int Q_TILE = 64 * D * 2;       // Q or dO tile
   static constexpr int DS_TILE = 128 * 64 * 2;    // dS^T tile, 128 keys x 64 queries, 16-bit
-  static constexpr int DQ_HALF = D * 128;         // dQ^T staging: D rows x 32 fp32 queries (128 B)
   static constexpr int STG = (D == 128) ? 4 : 6;  // Q/dO/lse/D stages
   static constexpr int THREADS = 512;
   // barrier indices
@@ -66,8 +68,16 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + STG * Q_TILE;         // [2] dS^T tiles (V first)
   static constexpr int OFF_V = OFF_DS;
   static_assert(2 * DS_TILE >= KV_TILE, "V fits in the dS^T buffers");
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;          // [2] dQ^T staging halves
-  static constexpr int OFF_LD = OFF_DQ + 2 * DQ_HALF;          // [STG][2][64] floats: -lse*log2e, -D
+  // d=64: dQ^T staged as two [d rows x 32 fp32 queries] halves (128-byte rows, 128-byte
+  // swizzle) for the TMA tensor reductions; d=128 adds from registers and stages nothing.
+  // The fp32 accumulator is [B*Hq, Npad, d] at d=128 and [B*Hq, d, Npad] at d=64.
+  static constexpr bool DQ_TMA = (D == 64);
+  // MMA issue order of a step's two products (see the MMA warp)
+  static constexpr bool DP_FIRST = (D == 128);
+  static constexpr int DQ_HALF = D * 128;
+  static constexpr int OFF_DQS = OFF_DS + 2 * DS_TILE;
+  static constexpr int DQS_BYTES = DQ_TMA ? 2 * DQ_HALF : 0;
+  static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;           // [STG][2][64] floats: -lse*log2e, -D
   static constexpr int OFF_BAR = OFF_LD + STG * 2 * 64 * 4;
   // no alignment slack: the dynamic shared-memory base is 1024-byte aligned (checked at
   // run time by the kernel)
@@ -111,6 +121,11 @@ __device__ __forceinline__ float bw_unpack_hi(uint32_t v) {
   return __half2float(__half(hr));
 }
 
+// global[p] += v, relaxed, without a result (a reduction, not a returning atomic)
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -121,7 +136,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // ------------------------------------------------------------------- preprocess
 // -D = -rowsum(dO * O) and -lse * log2(e) in the padded [B*Hq, Npad] layout (negated so
 // the main kernel adds them; 0 and -inf past N, which zeroes P for padded query rows);
-// zeroes the dQ accumulator ([B*Hq, d, Npad] fp32).
+// zeroes the fp32 dQ accumulator.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__ BwdParams p) {
   constexpr int LPR = D / 8;  // lanes per row, 8 elements (16 B) per lane
@@ -232,18 +247,53 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_varlen(const __grid_con
 }
 
 // ------------------------------------------------------------------ dQ convert
-// dQ[b, n, h, :] = scale * acc[b*Hq + h, :, n]: a tiled transpose through shared memory
-// (coalesced fp32 reads along n, coalesced 16-bit writes along d).
+// d=128: dQ[b, n, h, :] = scale * acc[b*Hq + h, n, :]: each thread converts 8 consecutive
+// elements of one row (two 16-byte reads, one 16-byte write); consecutive threads walk
+// the output in order, so the writes are contiguous and every read covers whole rows.
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__ BwdParams p) {
+  constexpr int TPR = D / 8;  // threads per row
+  const int nrow = VARLEN ? p.Npad : p.N;
+  const long long total = static_cast<long long>(p.B) * nrow * p.Hq * TPR;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const long long row = i / TPR;  // (b * nrow + n) * Hq + h
+    const int part = static_cast<int>(i % TPR);
+    const int h = static_cast<int>(row % p.Hq);
+    const long long bn = row / p.Hq;
+    const int n = static_cast<int>(bn % nrow);
+    const int b = static_cast<int>(bn / nrow);
+    long long orow = static_cast<long long>(b) * p.N + n;  // output row of query n
+    if (VARLEN) {
+      int sq = 0, lq = 0, sk = 0, lk = 0;
+      if (!seq_span(p.vl, b, sq, lq, sk, lk) || n >= lq) continue;
+      orow = sq + n;
+    }
+    const float4* src =
+        reinterpret_cast<const float4*>(p.dq_acc + (static_cast<long long>(b * p.Hq + h) * p.Npad + n) * D + 8 * part);
+    const float4 a = src[0], c = src[1];
+    const float sc = p.scale;
+    uint4 o;
+    o.x = bw_pack2<BF16>(a.x * sc, a.y * sc);
+    o.y = bw_pack2<BF16>(a.z * sc, a.w * sc);
+    o.z = bw_pack2<BF16>(c.x * sc, c.y * sc);
+    o.w = bw_pack2<BF16>(c.z * sc, c.w * sc);
+    *reinterpret_cast<uint4*>(p.dq + (orow * p.Hq + h) * D + 8 * part) = o;
+  }
+}
+
+// d=64: dQ[b, n, h, :] = scale * acc[b*Hq + h, :, n]: a tiled transpose through shared
+// memory (coalesced fp32 reads along n, coalesced 16-bit writes along d); one block per
+// (b*Hq + h, 64 queries).
+template <int D, bool BF16, bool VARLEN>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_t(const __grid_constant__ BwdParams p) {
   __shared__ float tile[D][65];
   const int nblk = VARLEN ? p.Npad / 64 : (p.N + 63) / 64;
   const int bh = static_cast<int>(blockIdx.x / nblk);
   const int n0 = 64 * static_cast<int>(blockIdx.x % nblk);
   const int b = bh / p.Hq, h = bh % p.Hq;
-  // output row of query n: b*N + n, or start_q + n of sequence b
   int len_q = p.N;
-  long long row0 = static_cast<long long>(b) * p.N;
+  long long row0 = static_cast<long long>(b) * p.N;  // output row of query 0 of this sequence
   if (VARLEN) {
     int sq = 0, sk = 0, lk = 0;
     if (!seq_span(p.vl, b, sq, len_q, sk, lk)) return;
@@ -286,7 +336,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* wg_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [4]
-  volatile int* dq_fail = reinterpret_cast<volatile int*>(tmem_slot + 6);  // dQ warpgroup gave up
+  volatile int* dq_fail = reinterpret_cast<volatile int*>(tmem_slot + 6);  // d=64 dQ warps gave up
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * i; };
@@ -396,7 +446,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         tma_prefetch_desc(&p.tm_do);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
-        tma_prefetch_desc(&p.tm_dq);
+        if (C::DQ_TMA && DQ) tma_prefetch_desc(&p.tm_dq);
         mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
         for (int ch = 0; ch < C::CHUNKS; ++ch) {
           if (VARLEN) {
@@ -467,33 +517,42 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
             ok = false;
             break;
           }
-          // S^T(it) overwrites the buffer that held dQ^T(it-2): it must have been read out
-          if (DQ && it >= 2 && !__all_sync(FULL, mbar_wait(dq_free, (it - 2) & 1, abort_flag, lim))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint64_t qs = u16(s * C::Q_TILE);
-          // S^T = K Q^T  (both K-major in shared memory)
-          if (leader) {
+          // S^T(it) overwrites the buffer that held dQ^T(it-2), which must have been read
+          // out; dP^T(it) overwrites the columns the previous step's softmax has loaded.
+          auto issue_s = [&]() {
+            if (DQ && it >= 2 && !__all_sync(FULL, mbar_wait(dq_free, (it - 2) & 1, abort_flag, lim))) return false;
+            tc_fence_after();
+            // S^T = K Q^T  (both K-major in shared memory)
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tbase + C::T_S + 64u * bb, dK_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
-                     dQ_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
-          }
-          if (it > 0 && !__all_sync(FULL, mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim))) {
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tbase + C::T_S + 64u * bb, dK_km + u16((kk / 4) * C::KV_CHUNK + (kk % 4) * 32),
+                       dQ_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
+            }
+            return true;
+          };
+          auto issue_dp = [&]() {
+            if (it > 0 && !__all_sync(FULL, mbar_wait(dp_free, (it - 1) & 1, abort_flag, lim))) return false;
+            tc_fence_after();
+            // dP^T = V dO^T  (V from TMEM as 16-bit pairs; dO K-major)
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ts(tbase + C::T_DP, tbase + C::T_V + 8u * kk,
+                       dDO_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
+            }
+            return true;
+          };
+          // Issue order, measured per head dimension on GB300: at d=128 dP^T first (it runs
+          // while the dQ warpgroup reads dQ^T(it-2) out of S^T's buffer; 4.29 against 4.51 ms
+          // for the 16k-token backward), at d=64 S^T first (6.48 against 6.78 ms).
+          const bool issued = C::DP_FIRST ? (issue_dp() && issue_s()) : (issue_s() && issue_dp());
+          if (!issued) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          // dP^T = V dO^T  (V from TMEM as 16-bit pairs; dO K-major)
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ts(tbase + C::T_DP, tbase + C::T_V + 8u * kk,
-                     dDO_km + qs + u16((kk / 4) * C::Q_CHUNK + (kk % 4) * 32), id_sdp, kk > 0);
-            mma_commit(sdp_full);
-          }
+          if (leader) mma_commit(sdp_full);  // covers both products
         }
         if (it > 0) {
           const int i = it - 1, s = i % C::STG, bb = i & 1;
@@ -704,17 +763,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   } else {
     setmaxnreg_dec<112>();
     // ------------------------------------------- dQ^T -> fp32 accumulator
-    // Thread r holds row d = r of dQ^T (64 query columns).  Each 32-query half is staged
-    // as [d rows x 128 B] with the 128-byte swizzle and added into the accumulator
-    // ([B*Hq, d, Npad] fp32, queries contiguous) by one TMA bulk tensor reduction.
+    // Thread r holds row d = r of dQ^T (64 query columns).  Once they are in registers the
+    // TMEM buffer is released, and they are added into the fp32 accumulator.  d=128
+    // ([B*Hq, Npad, d], d contiguous): one reduction per query, the 32 lanes of a warp
+    // covering 32 consecutive d (one aligned 128-byte line).  d=64 ([B*Hq, d, Npad], queries
+    // contiguous): each 32-query half is staged as [d rows x 128 B] with the 128-byte
+    // swizzle and added by one TMA tensor reduction.
     bool ok = true;
     for (int it = 0; it < (DQ ? T : 0); ++it) {  // without the dQ path only the dV epilogue
       const int hq = hkv * G + it / nq;
       const int q0 = 64 * (qb0 + it % nq);
-      // The named barriers below span the four warps of this warpgroup, but a wait's
-      // outcome is only warp-uniform: a warp that gives up records it in dq_fail and
-      // still arrives at the barrier, after which all four warps read the same flag and
-      // leave together (no warp is left waiting at a barrier the others skipped).
       const bool got = __all_sync(FULL, mbar_wait(dq_full(it & 1), (it >> 1) & 1, abort_flag, lim));
       uint32_t v[64];
       if (got) {
@@ -725,35 +783,47 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(dq_free);
-      } else if (lane == 0) {
-        *dq_fail = 1;
       }
-      if (r == 0) bulk_wait_group_read0();  // the previous step's reductions have read the staging
-      named_bar_sync_n(1, 128);
-      if (*dq_fail) {
-        ok = false;
-        break;
-      }
-      if (r < D) {
+      if constexpr (!C::DQ_TMA) {
+        if (!got) {
+          ok = false;
+          break;
+        }
+        float* dst = p.dq_acc + (static_cast<long long>(b * p.Hq + hq) * p.Npad + q0) * D + r;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint8_t* rowp = smem + C::OFF_DQ + hh * C::DQ_HALF + r * 128;
+        for (int c = 0; c < 64; ++c) red_add_f32(dst + c * D, __uint_as_float(v[c]));
+      } else {
+        // The named barriers span the four warps, but a wait's outcome is only
+        // warp-uniform: a warp that gives up records it in dq_fail and still arrives, after
+        // which all four read the same flag and leave together.
+        if (!got && lane == 0) *dq_fail = 1;
+        if (r == 0) bulk_wait_group_read0();  // the previous reduction has read the tile
+        named_bar_sync_n(1, 128);
+        if (*dq_fail) {
+          ok = false;
+          break;
+        }
+        if (r < D) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
-                make_uint4(v[32 * hh + 4 * u], v[32 * hh + 4 * u + 1], v[32 * hh + 4 * u + 2], v[32 * hh + 4 * u + 3]);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint8_t* rowp = smem + C::OFF_DQS + hh * C::DQ_HALF + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = make_uint4(
+                  v[32 * hh + 4 * u], v[32 * hh + 4 * u + 1], v[32 * hh + 4 * u + 2], v[32 * hh + 4 * u + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync_n(1, 128);
+        if (r == 0) {
+          const int bh = b * p.Hq + hq;
+          tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQS, q0, 0, bh);
+          tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQS + C::DQ_HALF, q0 + 32, 0, bh);
+          bulk_commit_group();
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync_n(1, 128);
-      if (r == 0) {
-        const int bh = b * p.Hq + hq;
-        tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQ, q0, 0, bh);
-        tma_reduce_add_3d(&p.tm_dq, sbase + C::OFF_DQ + C::DQ_HALF, q0 + 32, 0, bh);
-        bulk_commit_group();
-      }
     }
-    if (r == 0) bulk_wait_group0();
+    if (C::DQ_TMA && r == 0) bulk_wait_group0();
     // ---- epilogue: dV -> 16-bit rows
     if (!ok) {
       wg_fail[2] = 1;
@@ -826,11 +896,16 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     }
   }
   if (!DQ) return launch_bwd_dq(p, D, BF16 ? FA_BF16 : FA_FP16, CAUSAL, stream);
-  {
+  if (BwdCfg<D>::DQ_TMA) {
     const long long grid = static_cast<long long>(p.B) * p.Hq * (VARLEN ? p.Npad / 64 : (p.N + 63) / 64);
-    fa_bwd_dq_convert<D, BF16, VARLEN><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    fa_bwd_dq_convert_t<D, BF16, VARLEN><<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+  } else {
+    const long long threads = static_cast<long long>(p.B) * (VARLEN ? p.Npad : p.N) * p.Hq * (D / 8);
+    const long long want = (threads + 255) / 256;
+    const int grid = static_cast<int>(want < 16LL * sms ? (want > 0 ? want : 1) : 16LL * sms);
+    fa_bwd_dq_convert<D, BF16, VARLEN><<<grid, 256, 0, stream>>>(p);
   }
+  return cudaGetLastError();
 }
 
 template <int D, bool BF16>

@@ -60,14 +60,14 @@ bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d,
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
   CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
-  CUtensorMap tm_dq;        // fp32 dQ accumulator [B*Hq, d, Npad], box {32, d, 1}, 128-byte swizzle
+  CUtensorMap tm_dq;        // d=64: fp32 dQ accumulator [B*Hq, d, Npad], box {32, d, 1}, 128-byte swizzle
   const uint16_t* o;        // [B, N, Hq, d] (preprocess)
   const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
   const float* lse;         // [B, Hq, N]
   uint16_t* dq;             // [B, N, Hq, d]
   uint16_t* dk;             // [B, N, Hkv, d]
   uint16_t* dv;             // [B, N, Hkv, d]
-  float* dq_acc;            // workspace: fp32 [B*Hq, d, Npad] (queries contiguous)
+  float* dq_acc;            // workspace: fp32, [B*Hq, Npad, d] at d=128, [B*Hq, d, Npad] at d=64
   float* dvec;              // workspace: -D = -rowsum(dO*O), [B*Hq, Npad] (0 past N)
   float* l2vec;             // workspace: -lse * log2(e), [B*Hq, Npad] (-inf past N)
   unsigned* err;
@@ -125,7 +125,9 @@ struct BwdWorkspace {
 };
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int d);
 
-// 3-D map over the fp32 dQ accumulator [B*Hq, d, Npad], box = {32, d, 1}, 128-byte swizzle.
+
+// 3-D map over the fp32 dQ accumulator [BH, d, Npad] (queries contiguous), box {32, d, 1},
+// 128-byte swizzle: the target of the d=64 backward's tensor reductions.
 bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, int d);
 
 unsigned* device_error_word();  // address of this device's error word (device memory)

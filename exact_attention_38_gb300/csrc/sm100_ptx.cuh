@@ -130,20 +130,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase has not completed may be
+// parked for up to `ns` nanoseconds; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false when
 // `*abort` becomes non-zero (if `abort` is not null) or when more than `limit_ns`
 // nanoseconds pass; the caller then records the error and winds down instead of
-// spinning forever.
+// spinning forever.  Between checks the thread is parked on the barrier (up to 200 us
+// at a time), which measured faster than polling it.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_for(bar, parity, 200000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
