@@ -90,10 +90,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ accumulator
- * [B*Hq, d, Npad] (queries contiguous), then -D = -rowsum(dO * O) and -lse * log2(e),
- * each [B*Hq, Npad] fp32, with Npad = N rounded up to a multiple of 64; each part
- * rounded up to 256 bytes.
+ * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ accumulator of
+ * B*Hq*Npad*d elements ([B*Hq, Npad, d] at d=128, [B*Hq, d, Npad] at d=64), then
+ * -D = -rowsum(dO * O) and -lse * log2(e), each [B*Hq, Npad] fp32, with Npad = N rounded
+ * up to a multiple of 64; each part rounded up to 256 bytes.
  * Returns 0 for invalid or unsupported sizes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
@@ -164,7 +164,8 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
 /*
  * Workspace bytes for fa_bwd_varlen: the fa_bwd layout with N replaced by
  * max_seqlen_q (Npad = max_seqlen_q rounded up to 64, at least 64), i.e. an fp32 dQ
- * accumulator [B*Hq, d, Npad] plus two [B*Hq, Npad] fp32 vectors.  0 for invalid sizes.
+ * accumulator of B*Hq*Npad*d elements plus two [B*Hq, Npad] fp32 vectors.  0 for
+ * invalid sizes.
  */
 size_t fa_bwd_varlen_workspace_size(int B, int Hq, int max_seqlen_q, int d);
 
