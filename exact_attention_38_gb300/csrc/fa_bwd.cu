@@ -885,7 +885,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   }
   {
     auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
-    cudaError_t e = set_smem_limit_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM);
+    cudaError_t e = prepare_launch_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM, C::THREADS, 128 * 80 + 256 * 160 + 128 * 112);
     if (e != cudaSuccess) return e;
     const long long nk = VARLEN ? p.vl.max_k : p.N;
     const long long grid = ((nk + 127) / 128) * p.B * p.Hkv;

@@ -358,7 +358,7 @@ template <int D, bool BF16, bool CAUSAL>
 static cudaError_t launch_bwd_dq_t(const BwdParams& p, cudaStream_t stream) {
   using C = DqCfg<D>;
   auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
-  cudaError_t e = set_smem_limit_once<fa_bwd_dq_kernel<D, BF16, CAUSAL>>(C::SMEM);
+  cudaError_t e = prepare_launch_once<fa_bwd_dq_kernel<D, BF16, CAUSAL>>(C::SMEM, 384, 128 * 80 + 256 * 200);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((p.N + 127) / 128) * p.B * p.Hq;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);

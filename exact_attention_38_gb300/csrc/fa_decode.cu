@@ -566,7 +566,7 @@ template <int D, bool BF16, bool CAUSAL, bool DEEP = false>
 static cudaError_t launch_decode_t(const DecParams& p, cudaStream_t stream) {
   using C = DecCfg<D, DEEP>;
   auto kern = fa_decode_kernel<D, BF16, CAUSAL, DEEP>;
-  cudaError_t e = set_smem_limit_once<fa_decode_kernel<D, BF16, CAUSAL, DEEP>>(C::SMEM);
+  cudaError_t e = prepare_launch_once<fa_decode_kernel<D, BF16, CAUSAL, DEEP>>(C::SMEM, 256, 128 * 80 + 128 * 176);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.B) * p.Hkv * p.S;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);

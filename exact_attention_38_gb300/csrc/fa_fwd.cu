@@ -42,6 +42,11 @@ struct FwdCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int STAGES = (D == 128) ? 4 : 8;
   static constexpr int THREADS = 384;             // 2 softmax warpgroups + control warpgroup
+  // registers after setmaxnreg: control warpgroup 80, softmax warpgroups 208 each; the
+  // total must fit the launch allocation of 384 x 168 = 64512 (checked before launch)
+  static constexpr int REG_CTRL = 80, REG_SOFTMAX = 208;
+  static constexpr int REG_SPLIT = 128 * REG_CTRL + 256 * REG_SOFTMAX;
+  static_assert(REG_SPLIT <= 384 * 168, "register split above the launch allocation");
   static constexpr int NBARS = 8 + 2 * STAGES + 1;
   static constexpr int SMEM = 1024 + TILES * TILE_BYTES + STAGES * TILE_BYTES + 8 * NBARS + 64;
   static constexpr uint32_t TMEM_COLS = 512;      // S_0, S_1 (128 each), O_0, O_1 (D each)
@@ -163,8 +168,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
   };
 
   if (warp >= 8) {
-   // control warpgroup gives registers to the softmax warpgroups
-   setmaxnreg_dec<80>();
+   // control warpgroup gives registers to the softmax warpgroups (C::REG_SPLIT)
+   setmaxnreg_dec<C::REG_CTRL>();
    // The control warps run their loops with all 32 lanes (warp-uniform control flow,
    // so loop state and descriptors live in uniform registers); one elected lane issues
    // the TMA copies, the tcgen05 instructions and their commits.
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
     __syncwarp();
    }
   } else {
-    setmaxnreg_inc<208>();
+    setmaxnreg_inc<C::REG_SOFTMAX>();
     // ----------------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;
     const int rit = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
@@ -477,7 +482,7 @@ template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>;
-  cudaError_t e = set_smem_limit_once<fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>>(C::SMEM);
+  cudaError_t e = prepare_launch_once<fa_fwd_kernel<D, BF16, CAUSAL, VARLEN>>(C::SMEM, C::THREADS, C::REG_SPLIT);
   if (e != cudaSuccess) return e;
   const long long nqb = ((VARLEN ? p.vl.max_q : p.N) + 255) / 256;
   const long long grid = nqb * p.B * p.Hq;

@@ -414,8 +414,9 @@ cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream)
     if (e != cudaSuccess) return e;
   }
   auto kern = causal ? fa_fwd_fp8_kernel<true> : fa_fwd_fp8_kernel<false>;
-  cudaError_t e = causal ? set_smem_limit_once<fa_fwd_fp8_kernel<true>>(kSmem)
-                         : set_smem_limit_once<fa_fwd_fp8_kernel<false>>(kSmem);
+  constexpr int kSplit = 128 * 80 + 256 * 208;
+  cudaError_t e = causal ? prepare_launch_once<fa_fwd_fp8_kernel<true>>(kSmem, 384, kSplit)
+                         : prepare_launch_once<fa_fwd_fp8_kernel<false>>(kSmem, 384, kSplit);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((p.N + 255) / 256) * p.B * p.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, kSmem, stream>>>(p);

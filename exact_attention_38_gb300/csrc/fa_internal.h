@@ -132,18 +132,31 @@ bool encode_dq_acc_map(CUtensorMap* map, const float* base, int BH, int Npad, in
 
 unsigned* device_error_word();  // address of this device's error word (device memory)
 
-// Raises kernel `Kern`'s dynamic shared-memory limit to `bytes`, once per device: the
-// attribute belongs to the function on the current device and stays set, so repeating
-// it on every launch only costs host time.  (Devices 64 and up repeat it every call.)
+// First-launch preparation of kernel `Kern` on the current device, done once per device:
+//  - raises its dynamic shared-memory limit to `smem_bytes` (the attribute belongs to the
+//    function on the device and stays set, so repeating it per launch only costs time);
+//  - checks its register split: a kernel whose warpgroups rebalance registers with
+//    setmaxnreg needs `split_regs` registers in total (threads x registers of every role
+//    after the rebalancing), and setmaxnreg.inc draws only on the block's own launch
+//    allocation (threads x the compiled register count, in steps of 8 per thread).  A
+//    split above that would make setmaxnreg.inc wait forever, so the launch is refused.
+// (Devices 64 and up repeat the preparation on every call.)
 template <auto Kern>
-cudaError_t set_smem_limit_once(int bytes) {
+cudaError_t prepare_launch_once(int smem_bytes, int threads, int split_regs) {
   static std::atomic<unsigned long long> done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
   if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
-  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (split_regs > 0) {
+    cudaFuncAttributes attr{};
+    e = cudaFuncGetAttributes(&attr, Kern);
+    if (e != cudaSuccess) return e;
+    const long long per_thread = (static_cast<long long>(attr.numRegs) + 7) / 8 * 8;
+    if (per_thread * threads < split_regs) return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
