@@ -3,6 +3,7 @@
 // an error code without touching the device (and works on a host without a GPU).
 #include "fa_decode_policy.h"
 #include "fa_internal.h"
+#include "fa_math.cuh"
 #include "sm100_ptx.cuh"
 
 #include <cuda.h>
@@ -254,6 +255,22 @@ __global__ void fa_selftest_wait_kernel(unsigned* err, uint64_t limit_ns) {
   __syncthreads();
   const bool ok = mbar_wait(smem_u32(&bar), 0, nullptr, limit_ns);
   if (!ok && threadIdx.x == 0) atomicOr(err, kDevErrTimeout);
+}
+
+// Evaluates both exponential forms the softmax kernels use, element by element.
+__global__ void fa_selftest_exp2_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
+  const long long i = 2LL * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const bool two = i + 1 < n;
+  const float x0 = x[i], x1 = two ? x[i + 1] : 0.f;
+  float p0, p1;
+  f2unpack(ex2_poly2(f2pack(x0, x1)), p0, p1);
+  y_poly[i] = p0;
+  y_mufu[i] = ex2_mufu(x0);
+  if (two) {
+    y_poly[i + 1] = p1;
+    y_mufu[i + 1] = ex2_mufu(x1);
+  }
 }
 
 }  // namespace fa
@@ -614,6 +631,17 @@ fa_status fa_selftest_wait_timeout(int limit_us, fa_stream_t stream) {
   if (!err) return FA_ERR_CUDA;
   fa_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err,
                                                                                static_cast<uint64_t>(limit_us) * 1000);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_selftest_exp2(const float* x, float* y_poly, float* y_mufu, int n, fa_stream_t stream) {
+  if (n < 0) return FA_ERR_INVALID;
+  if (n == 0) return FA_OK;
+  if (!aligned4(x) || !aligned4(y_poly) || !aligned4(y_mufu)) return FA_ERR_INVALID;
+  const long long threads = (static_cast<long long>(n) + 1) / 2;
+  const long long grid = (threads + 255) / 256;
+  fa_selftest_exp2_kernel<<<static_cast<unsigned>(grid), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      x, y_poly, y_mufu, n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

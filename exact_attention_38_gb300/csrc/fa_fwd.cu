@@ -25,6 +25,7 @@
 //    and TMA-stores it (rows >= N are clipped by the tensor map), and writes
 //    lse = scale * m + ln(l).
 #include "fa_internal.h"
+#include "fa_math.cuh"
 #include "sm100_ptx.cuh"
 
 #include <cuda_bf16.h>
@@ -53,11 +54,7 @@ struct FwdCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+__device__ __forceinline__ float ex2f(float x) { return ex2_mufu(x); }
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {

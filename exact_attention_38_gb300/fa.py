@@ -68,6 +68,8 @@ def _load():
     lib.fa_fwd_fp8_workspace_size.restype = sz
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_selftest_exp2.argtypes = [vp, vp, vp, i, vp]
+    lib.fa_selftest_exp2.restype = i
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i
     lib.fa_status_string.argtypes = [i]

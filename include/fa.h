@@ -328,6 +328,20 @@ fa_status fa_check_device_error(fa_stream_t stream);
  */
 fa_status fa_selftest_wait_timeout(int limit_us, fa_stream_t stream);
 
+/*
+ * Self-test of the exponentials the softmax kernels use: for each of the n fp32 inputs
+ * x[i] (DEVICE pointers, 4-byte aligned, n >= 0), y_poly[i] receives 2^x[i] from the
+ * polynomial form evaluated on the FMA pipe (round-to-nearest range reduction
+ * x = n + f, f in [-1/2, 1/2], and a degree-3 polynomial for 2^f exact at f = 0; relative
+ * error below 1.1e-4 for -125 <= x <= 8, exact at integers, exactly 0 below -125) and y_mufu[i] receives
+ * the special-function unit's ex2.approx.ftz result, which the attention kernels use.  The
+ * polynomial form is an alternative for kernels whose special-function unit is the bound;
+ * in this library's forward it measured slower, so no kernel uses it.  The library's own
+ * tests compare both forms with the exact value.  Returns FA_OK once
+ * enqueued, FA_ERR_INVALID for a negative n or a misaligned pointer.
+ */
+fa_status fa_selftest_exp2(const float* x, float* y_poly, float* y_mufu, int n, fa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 
