@@ -92,7 +92,7 @@ def kernel_source_digest(kernel):
     import hashlib
 
     csrc = os.path.join(ROOT, "exact_attention_38_gb300", "csrc")
-    files = {"fa_fwd_kernel": ["fa_fwd.cu"], "fa_bwd_main": ["fa_bwd.cu"]}[kernel]
+    files = {"fa_fwd_kernel": ["fa_fwd.cu", "fa_math.cuh", "exp2_poly.h"], "fa_bwd_main": ["fa_bwd.cu"]}[kernel]
     h = hashlib.sha256()
     for f in files + ["sm100_ptx.cuh", "fa_internal.h"]:
         with open(os.path.join(csrc, f), "rb") as fh:
