@@ -320,6 +320,53 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_t(const __grid_constant
   }
 }
 
+// ------------------------------------------------------------- dK / dV epilogue
+// Writes the 128-key tile held in TMEM columns [col, col + D) (thread r = key row r, fp32),
+// times `mul`, as 16-bit rows.  Fixed length: through a shared-memory tile laid out as the
+// K/V loads (64-column chunks of 128 rows x 128 B, 128-byte swizzle) and TMA tensor stores,
+// which clip rows past N; the 128 threads of the calling warpgroup take part (named barrier
+// `bar_id`).  Variable length: row by row (a tile store could run into the next sequence).
+template <int D, bool BF16, bool VARLEN>
+__device__ __forceinline__ void bwd_write_tile(uint32_t tm, float mul, uint8_t* stage, const CUtensorMap* map,
+                                               uint16_t* out_row, bool live, int bar_id, int r, int hkv, int k0,
+                                               int b) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tm + 32u * c, v);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = bw_pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    if (VARLEN) {
+      if (live) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(out_row + 32 * c + 8 * u) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+    } else {
+      uint8_t* rowp = stage + (c >> 1) * (128 * 128) + r * 128;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int unit = (c & 1) * 4 + u;
+        *reinterpret_cast<uint4*>(rowp + ((unit ^ (r & 7)) * 16)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+    }
+  }
+  if (!VARLEN) {
+    fence_proxy_async_smem();
+    named_bar_sync_n(bar_id, 128);
+    if (r == 0) {
+#pragma unroll
+      for (int ch = 0; ch < D / 64; ++ch) tma_store_4d(map, smem_u32(stage + ch * (128 * 128)), ch * 64, hkv, k0, b);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the staging must outlive the copy's reads of it
+    }
+  }
+}
+
 // ------------------------------------------------------------------- main kernel
 template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
 __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
@@ -447,6 +494,10 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         if (C::DQ_TMA && DQ) tma_prefetch_desc(&p.tm_dq);
+        if (!VARLEN) {
+          tma_prefetch_desc(&p.tm_dk);
+          tma_prefetch_desc(&p.tm_dv);
+        }
         mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
         for (int ch = 0; ch < C::CHUNKS; ++ch) {
           if (VARLEN) {
@@ -740,24 +791,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       if (wg_fail[0] == 0) {
         tc_fence_after();
         const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
-        uint16_t* out = p.dk + (krow * p.Hkv + hkv) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::T_DK + 32u * c, v);
-          tmem_wait_ld();
-          if (key < len_k) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint4 o;
-              o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]) * p.scale, __uint_as_float(v[8 * u + 1]) * p.scale);
-              o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]) * p.scale, __uint_as_float(v[8 * u + 3]) * p.scale);
-              o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]) * p.scale, __uint_as_float(v[8 * u + 5]) * p.scale);
-              o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]) * p.scale, __uint_as_float(v[8 * u + 7]) * p.scale);
-              *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
-            }
-          }
-        }
+        bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DK, p.scale, smem + C::OFF_Q, &p.tm_dk,
+                                        p.dk + (krow * p.Hkv + hkv) * D, key < len_k, 2, r, hkv, k0, b);
       }
     }
   } else {
@@ -838,24 +873,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       tc_fence_after();
       const int key = k0 + r;
       const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
-      uint16_t* out = p.dv + (krow * p.Hkv + hkv) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + C::T_DV + 32u * c, v);
-        tmem_wait_ld();
-        if (key < len_k) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 o;
-            o.x = bw_pack2<BF16>(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-            o.y = bw_pack2<BF16>(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-            o.z = bw_pack2<BF16>(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-            o.w = bw_pack2<BF16>(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-            *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
-          }
-        }
-      }
+      bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DV, 1.0f, smem + C::OFF_DO, &p.tm_dv,
+                                      p.dv + (krow * p.Hkv + hkv) * D, key < len_k, 3, r, hkv, k0, b);
     }
   }
 

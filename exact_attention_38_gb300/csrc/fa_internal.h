@@ -60,6 +60,7 @@ bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d,
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
   CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
+  CUtensorMap tm_dk, tm_dv; // fixed length: outputs [B, N, Hkv, d], box rows 128 (TMA stores)
   CUtensorMap tm_dq;        // d=64: fp32 dQ accumulator [B*Hq, d, Npad], box {32, d, 1}, 128-byte swizzle
   const uint16_t* o;        // [B, N, Hq, d] (preprocess)
   const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
