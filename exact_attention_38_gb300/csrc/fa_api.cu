@@ -302,6 +302,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.err = device_error_word();
   if (!p.err) return FA_ERR_CUDA;
   p.lse = lse;
+  p.o = static_cast<uint16_t*>(o);
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -309,7 +310,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = kWaitLimitNs;
-  const cudaError_t e = launch_fwd(p, d, dtype, causal != 0, false, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool persistent = N <= (causal ? kPersistentMaxNCausal : kPersistentMaxN);
+  const cudaError_t e = persistent ? launch_fwd_persistent(p, d, dtype, causal != 0, s)
+                                   : launch_fwd(p, d, dtype, causal != 0, false, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -166,6 +166,20 @@ cudaError_t prepare_launch_once(int smem_bytes, int threads, int split_regs) {
 int device_sm_count();
 
 cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
+// Persistent forward (fixed length): one CTA per SM takes units from a counter pair
+// {next, done} in device memory.  Each launch takes the next pair of a ring of
+// kSchedSlots per device (round robin over all launches of the process); the launch's
+// last CTA puts the pair back to {0, 0}.  Two launches that use one pair at the same time
+// (kSchedSlots launches apart, still running together) would share its units.
+constexpr int kSchedSlots = 256;
+// fa_fwd runs the persistent kernel up to these sequence lengths (few key blocks per unit,
+// where a unit's start and finish cost as much as its blocks) and one CTA per unit above;
+// both limits are where the persistent kernel stopped measuring faster
+constexpr int kPersistentMaxN = 512;
+constexpr int kPersistentMaxNCausal = 1024;
+constexpr int kMaxSchedDevices = 64;
+unsigned* scheduler_slot();  // nullptr if the device's ring cannot be found
+cudaError_t launch_fwd_persistent(const FwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
 // deterministic: dK/dV from the key-block kernel without its dQ path, then dQ from the
 // query-tile kernel (fa_bwd_dq.cu) in a fixed summation order; p.dq_acc must be null.
 cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, bool deterministic,

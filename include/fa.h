@@ -41,17 +41,18 @@
  *    device, including one that has not finished when the check reads the word.
  *  - Calls on different streams may overlap; the library keeps no per-call state,
  *    except fa_bwd_noalloc, whose calls all share one scratch array and must be
- *    serialised (see there).
- *  - Per device the library remembers a few addresses and settings (the error word's
- *    and fa_bwd_noalloc's scratch addresses, each kernel's shared-memory limit), taken
- *    on the first call that needs them.  cudaDeviceReset() discards them on the device
+ *    serialised (see there), and fa_fwd's persistent kernel, whose launches each take
+ *    a counter pair from a ring of 256 (see fa_fwd).
+ *  - Per device the library remembers a few addresses and settings (the error word's,
+ *    the counter ring's and fa_bwd_noalloc's scratch addresses, each kernel's
+ *    shared-memory limit), taken on the first call that needs them.  cudaDeviceReset() discards them on the device
  *    side, so the library must not be used on a device after cudaDeviceReset() in the
  *    same process.
  *  - The compute entry points may be captured into a CUDA graph and replayed (their
  *    host-side work, tensor-map encoding and launch attributes, happens at capture and
  *    is baked into the graph's kernel parameters; the buffers must then stay at the
  *    captured addresses).  Make one call on the device before capturing: the first
- *    call looks up the device's error word.  fa_check_device_error synchronises and
+ *    call looks up the device's error word and counter ring.  fa_check_device_error synchronises and
  *    cannot be captured.
  */
 #ifndef FA_H_
@@ -84,6 +85,12 @@ typedef enum fa_dtype { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
  * O is rounded to nearest into `dtype` from an fp32 accumulator.  The kernel is
  * exact attention: it differs from the plain definition only by rounding
  * ("Bloques pequeños, normalización global").
+ * Short sequences (N <= 512, or N <= 1024 with the mask) run a persistent kernel: one
+ * CTA per SM takes (batch, head, 256-query) units from a counter pair in device memory,
+ * one pair per launch from a ring of 256 per device, put back to zero by the launch's
+ * last CTA.  Launches that overlap in time get different pairs unless 256 launches
+ * separate them; a CUDA graph keeps the pair it was captured with.  Longer sequences
+ * run one CTA per unit.  Both kernels round the same operations in the same order.
  * Returns FA_OK once the work is enqueued.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
