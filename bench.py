@@ -467,12 +467,21 @@ def run_native(a):
     dom = max(per, key=lambda n: statistics.mean(per[n]))
     dom_ms = statistics.mean(per[dom])
     achieved = flops(w, dom) / (dom_ms * 1e-3) / 1e12
-    kern = "fa_fwd_kernel" if dom == "fwd" else "fa_bwd_main"
-    roofline = {"bound": "tensor", "kernel": kern,
-                "timed": "one fa_fwd call (one launch)" if dom == "fwd" else
-                         "one fa_bwd call: preprocess + fa_bwd_main + dQ convert (the main kernel is ~99% of it)",
+    if dom == "fwd":
+        # fa_fwd runs its persistent kernel for N <= 512 (N <= 1024 with the mask)
+        short = w["N"] <= (1024 if w.get("causal") else 512)
+        kern, timed = ("fa_fwd_persistent" if short else "fa_fwd_kernel"), "one fa_fwd call (one launch)"
+    elif w.get("deterministic"):
+        kern = "fa_bwd_main+fa_bwd_dq_kernel"
+        timed = ("one fa_bwd_deterministic call: preprocess + fa_bwd_main without its dQ path + fa_bwd_dq_kernel "
+                 "(FLOPs by the 2.5x backward count; the two kernels execute 3.5x the forward's)")
+    else:
+        kern = "fa_bwd_main"
+        timed = "one fa_bwd call: preprocess + fa_bwd_main + dQ convert (the main kernel is ~99% of it)"
+    roofline = {"bound": "tensor", "kernel": kern, "timed": timed,
                 "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                "traffic": recorded_traffic(kern, workload_name(w, "step")),
+                "traffic": (recorded_traffic(kern, workload_name(w, "step"))
+                            if kern in ("fa_fwd_kernel", "fa_bwd_main") else None),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                 "peak_kind": f"{peak_kind} bf16 dense, burst (of measured)"}
     passes = {n: {"ms": statistics.mean(per[n]), "ms_min": min(per[n]),
