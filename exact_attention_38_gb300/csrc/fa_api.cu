@@ -151,6 +151,42 @@ unsigned* device_error_word() {
   return p;
 }
 
+bool side_stream_fork(cudaStream_t stream, cudaStream_t* side, cudaEvent_t* join) {
+  struct Side {
+    cudaStream_t stream;
+    cudaEvent_t ev[kSideEvents][2];
+  };
+  static std::atomic<Side*> state[kMaxDevices];
+  static std::mutex mu;
+  static std::atomic<unsigned> next{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  Side* st = state[dev].load(std::memory_order_acquire);
+  if (!st) {
+    std::lock_guard<std::mutex> lock(mu);
+    st = state[dev].load(std::memory_order_acquire);
+    if (!st) {
+      Side* n = new Side{};
+      bool ok = cudaStreamCreateWithFlags(&n->stream, cudaStreamNonBlocking) == cudaSuccess;
+      for (int i = 0; i < kSideEvents && ok; ++i)
+        for (int j = 0; j < 2 && ok; ++j)
+          ok = cudaEventCreateWithFlags(&n->ev[i][j], cudaEventDisableTiming) == cudaSuccess;
+      if (!ok) {
+        cudaGetLastError();
+        return false;  // (the partly created set is left in place; this happens at most once)
+      }
+      state[dev].store(n, std::memory_order_release);
+      st = n;
+    }
+  }
+  const unsigned i = next.fetch_add(1u, std::memory_order_relaxed) % kSideEvents;
+  if (cudaEventRecord(st->ev[i][0], stream) != cudaSuccess || cudaStreamWaitEvent(st->stream, st->ev[i][0], 0) != cudaSuccess)
+    return false;
+  *side = st->stream;
+  *join = st->ev[i][1];
+  return true;
+}
+
 int device_sm_count() {
   static std::atomic<int> cached[kMaxDevices];
   int dev = 0;

@@ -902,18 +902,37 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // Deterministic pass: the dQ kernel reads only what the preprocess wrote, not the dK / dV
+  // kernel's output, so it runs on the library's side stream, launched first (its CTAs are
+  // the longer ones), while the dK / dV kernel runs on the caller's stream: each kernel's CTAs
+  // then fill the SMs the other's last wave leaves idle.  The caller's stream waits for both.
+  cudaStream_t side = nullptr;
+  cudaEvent_t join = nullptr;
+  cudaError_t e_side = cudaSuccess;
+  if (!DQ && side_stream_fork(stream, &side, &join)) {
+    e_side = launch_bwd_dq(p, D, BF16 ? FA_BF16 : FA_FP16, CAUSAL, side);
+    const cudaError_t ej = cudaEventRecord(join, side);
+    if (e_side == cudaSuccess) e_side = ej;
+  }
+  cudaError_t e_main = cudaSuccess;
   {
     auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
-    cudaError_t e = prepare_launch_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM, C::THREADS, 128 * 80 + 256 * 160 + 128 * 112);
-    if (e != cudaSuccess) return e;
+    e_main = prepare_launch_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM, C::THREADS, 128 * 80 + 256 * 160 + 128 * 112);
     const long long nk = VARLEN ? p.vl.max_k : p.N;
     const long long grid = ((nk + 127) / 128) * p.B * p.Hkv;
-    if (grid > 0) {
+    if (e_main == cudaSuccess && grid > 0) {
       kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
+      e_main = cudaGetLastError();
     }
   }
+  if (side) {
+    // join: the caller's stream goes on only once the side stream's dQ kernel is done
+    const cudaError_t ew = cudaStreamWaitEvent(stream, join, 0);
+    if (e_side != cudaSuccess) return e_side;
+    if (e_main != cudaSuccess) return e_main;
+    return ew;
+  }
+  if (e_main != cudaSuccess) return e_main;
   if (!DQ) return launch_bwd_dq(p, D, BF16 ? FA_BF16 : FA_FP16, CAUSAL, stream);
   if (BwdCfg<D>::DQ_TMA) {
     const long long grid = static_cast<long long>(p.B) * p.Hq * (VARLEN ? p.Npad / 64 : (p.N + 63) / 64);

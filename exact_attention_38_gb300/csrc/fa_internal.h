@@ -164,6 +164,14 @@ cudaError_t prepare_launch_once(int smem_bytes, int threads, int split_regs) {
 
 // Streaming-multiprocessor count of the current device (looked up once per device).
 int device_sm_count();
+// Fork for two independent launches: after this call, work enqueued on *side starts only
+// once the work enqueued on `stream` so far has finished; the caller then records *join on
+// *side and makes `stream` wait for it.  The side stream (non-blocking) and a ring of
+// kSideEvents event pairs are created once per device; calls that overlap in time get
+// different pairs unless kSideEvents calls separate them.  Returns false (nothing enqueued)
+// if the device's side stream or events cannot be had; the caller then stays on `stream`.
+constexpr int kSideEvents = 64;
+bool side_stream_fork(cudaStream_t stream, cudaStream_t* side, cudaEvent_t* join);
 
 cudaError_t launch_fwd(const FwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, cudaStream_t stream);
 // Persistent forward (fixed length): one CTA per SM takes units from a counter pair

@@ -41,11 +41,13 @@
  *    device, including one that has not finished when the check reads the word.
  *  - Calls on different streams may overlap; the library keeps no per-call state,
  *    except fa_bwd_noalloc, whose calls all share one scratch array and must be
- *    serialised (see there), and fa_fwd's persistent kernel, whose launches each take
- *    a counter pair from a ring of 256 (see fa_fwd).
+ *    serialised (see there), fa_fwd's persistent kernel, whose launches each take a
+ *    counter pair from a ring of 256 (see fa_fwd), and fa_bwd_deterministic, whose calls
+ *    each take an event pair from a ring of 64 for its side stream (see there).
  *  - Per device the library remembers a few addresses and settings (the error word's,
  *    the counter ring's and fa_bwd_noalloc's scratch addresses, each kernel's
- *    shared-memory limit), taken on the first call that needs them.  cudaDeviceReset() discards them on the device
+ *    shared-memory limit, the deterministic backward's side stream and events), taken on
+ *    the first call that needs them.  cudaDeviceReset() discards them on the device
  *    side, so the library must not be used on a device after cudaDeviceReset() in the
  *    same process.
  *  - The compute entry points may be captured into a CUDA graph and replayed (their
@@ -254,7 +256,10 @@ fa_status fa_fwd_decode_paged(const void* q, const void* k_pages, const void* v_
  * tensor memory: seven GEMM-shaped products per (query, key) block instead of five.
  * The pages mention no deterministic mode; this is the plain way to get one without
  * atomics or cross-block waits.  workspace as for fa_bwd (only its D and lse parts are
- * used).
+ * used).  The dQ kernel needs only D and lse, so it runs on a non-blocking stream of the
+ * library's (one per device) while the dK/dV kernel runs on `stream`; `stream` waits for
+ * it before anything enqueued after the call (event fork and join, which CUDA graph
+ * capture records as graph edges).
  */
 fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
