@@ -72,3 +72,28 @@ def test_bitwise_repeatable_and_dkdv_match(fa_lib, causal):
         ref = oracle.attn_bwd_dq_rows(xo["q"], xo["k"], xo["v"], xo["do"], causal, scale, 1, h, rows)
         got = f64(runs[0][0][1, rows, h, :].cpu())
         assert_close("dq", got, ref, ATOL["bf16"], "bf16")
+
+
+@pytest.mark.parametrize("d,H,causal", [(128, 16, False), (128, 16, True), (64, 32, False)])
+def test_bench_workload_16k_sampled(fa_lib, d, H, causal):
+    """The `--deterministic` bench workload (B=1, N=16384): dQ on sampled rows of two heads
+    against the oracle (the K / V rings wrap many times per CTA here), dK and dV equal to
+    fa_bwd's bit for bit."""
+    fa = fa_lib
+    B, N = 1, 16384
+    x = make_inputs(B, N, H, H, d, dtype="bf16", seed=320 + d + causal)
+    q, k, v, do = (to_gpu(x[n]) for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(do, q, k, v, o, lse, causal=causal, scale=scale, deterministic=True)
+    _, dk_nd, dv_nd = fa.backward(do, q, k, v, o, lse, causal=causal, scale=scale)
+    fa.check_device_error()
+    assert torch.equal(dk, dk_nd) and torch.equal(dv, dv_nd)
+    dq_host = dq.cpu()
+    del dq, dk, dv, dk_nd, dv_nd, o, lse
+    torch.cuda.empty_cache()
+    xo = {n: f64(t) for n, t in x.items()}
+    for h in (0, H - 1):
+        rows = sample_rows(N, 40, 330 + h)
+        ref = oracle.attn_bwd_dq_rows(xo["q"], xo["k"], xo["v"], xo["do"], causal, scale, 0, h, rows)
+        assert_close(f"dq h{h}", f64(dq_host[0, rows, h, :]), ref, ATOL["bf16"], "bf16")
