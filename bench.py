@@ -59,6 +59,8 @@ def parse():
                     help="with --decode: the caches as 128-row pages in a shuffled order behind a block table")
     ap.add_argument("--fp8", action="store_true",
                     help="forward only with E4M3 q, k, v (per-tensor descales), bf16 output")
+    ap.add_argument("--block-scales", action="store_true",
+                    help="with --fp8: one descale per 128-row block of each head (fa_fwd_fp8_blockscaled)")
     ap.add_argument("--Nq", type=int, default=1)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--min-len", type=int, default=512)
@@ -726,13 +728,15 @@ def run_fp8(a):
     import torch
 
     from exact_attention_38_gb300 import fa
-    from exact_attention_38_gb300.inputs import make_fp8_inputs
+    from exact_attention_38_gb300.inputs import make_fp8_block_inputs, make_fp8_inputs
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     w = workload(a)
     B, Hq, Hkv, N, d, causal = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"], w["causal"]
-    x = make_fp8_inputs(B, N, Hq, Hkv, d, seed=3)
+    blk = bool(getattr(a, "block_scales", False))
+    x = make_fp8_block_inputs(B, N, Hq, Hkv, d, seed=3) if blk else make_fp8_inputs(B, N, Hq, Hkv, d, seed=3)
+    bs = {n: x[n + "_descale"].to(dev) for n in ("q", "k", "v")} if blk else None
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
@@ -743,8 +747,14 @@ def run_fp8(a):
     scale = 1.0 / math.sqrt(d)
 
     def fwd():
-        st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, d,
-                           causal, scale, x["q_descale"], x["k_descale"], x["v_descale"], ws.data_ptr(), ws_bytes, sp)
+        if blk:
+            st = fa.fa_fwd_fp8_blockscaled(q.data_ptr(), k.data_ptr(), v.data_ptr(), bs["q"].data_ptr(),
+                                           bs["k"].data_ptr(), bs["v"].data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq,
+                                           Hkv, N, d, causal, scale, ws.data_ptr(), ws_bytes, sp)
+        else:
+            st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N,
+                               d, causal, scale, x["q_descale"], x["k_descale"], x["v_descale"], ws.data_ptr(),
+                               ws_bytes, sp)
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd_fp8")
 
@@ -770,7 +780,8 @@ def run_fp8(a):
     line = {"metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic",
-            "config": {"workload": workload_name(w, "fwd").replace("bf16", "e4m3 in, bf16 out"),
+            "config": {"workload": workload_name(w, "fwd").replace(
+                "bf16", "e4m3 in (descales per 128-row block and head), bf16 out" if blk else "e4m3 in, bf16 out"),
                        "l2": "flushed between steps (outside the timed events)"},
             "roofline": {"bound": "tensor", "kernel": "fa_fwd_fp8_kernel (+ V transpose)", "achieved": tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,

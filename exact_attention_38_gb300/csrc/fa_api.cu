@@ -615,6 +615,46 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, const float* q_descale,
+                                 const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq,
+                                 int Hkv, int N, int d, int causal, float scale, void* workspace,
+                                 size_t workspace_bytes, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+  if (q_descale == nullptr || k_descale == nullptr || v_descale == nullptr) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q_descale) | reinterpret_cast<uintptr_t>(k_descale) |
+       reinterpret_cast<uintptr_t>(v_descale)) & 3u)
+    return FA_ERR_INVALID;
+  const fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, FA_BF16);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < fa_fwd_fp8_workspace_size(B, Hkv, N, d))
+    return FA_ERR_INVALID;
+  Fp8Params p{};
+  p.Npad = (N + 127) / 128 * 128;
+  if (!encode_bshd_u8_map(&p.tm_q, q, B, N, Hq, d, 128) || !encode_bshd_u8_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
+      !encode_vt_u8_map(&p.tm_vt, workspace, B * Hkv, d, p.Npad))
+    return FA_ERR_CUDA;
+  p.err = device_error_word();
+  if (!p.err) return FA_ERR_CUDA;
+  p.v = static_cast<const uint8_t*>(v);
+  p.vt = static_cast<uint8_t*>(workspace);
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.q_bs = q_descale;
+  p.k_bs = k_descale;
+  p.v_bs = v_descale;
+  p.nb = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kWaitLimitNs;
+  const cudaError_t e = launch_fwd_fp8(p, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_fwd_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
                               const int* cache_seqlens, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                               int num_pages, int max_pages, int d, int causal, float scale, int num_splits,

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256) fa_fp8_transpose_v(const __grid_constant_
   }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool BLOCK>
 __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
   extern __shared__ uint8_t smem_raw_f8[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_f8) + 1023) & ~uintptr_t(1023));
@@ -299,6 +299,24 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
     const float cl2 = p.score_log2;
     const int row = r0_of(t) + rit;
     float m = -INFINITY, l = 0.f;
+    // Per-block descales: the score multiplier changes from key block to key block, so m is
+    // kept in log2 units of the scaled score (not of the raw product), and V's descale of
+    // block j enters P's exponent as log2(v_j / v_max) <= 0, v_max the largest over the
+    // tile's blocks: P * 2^7 * v_j / v_max still fits E4M3, l sums P without that factor
+    // (its block sum is divided by v_j / v_max), and O / l is multiplied by v_max.
+    float q_ds = 0.f, v_max = 0.f, v_inv = 0.f, k_next = 0.f, v_next = 0.f;
+    const int kvb = BLOCK ? (b * p.Hkv + hkv) * p.nb : 0;  // this head's first block descale
+    if constexpr (BLOCK) {
+      if (n_of(t) > 0) {
+        q_ds = p.q_bs[(b * p.Hq + h) * p.nb + (r0_of(t) >> 7)];
+        for (int j = lane; j < n_of(t); j += 32) v_max = fmaxf(v_max, p.v_bs[kvb + j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v_max = fmaxf(v_max, __shfl_xor_sync(FULL, v_max, o));
+        v_inv = 1.0f / v_max;
+        k_next = p.k_bs[kvb];  // block j's descales are read one block ahead
+        v_next = p.v_bs[kvb];
+      }
+    }
     bool ok = true;
     for (int j = 0; j < n_of(t); ++j) {
       if (!__all_sync(FULL, mbar_wait(s_full(t), j & 1, abort_flag, lim))) {
@@ -318,12 +336,24 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
         for (int c = 0; c < 128; ++c)
           if (c >= nvis) s[c] = -INFINITY;
       }
-      const float mx = rowmax128(s);
+      // score multiplier to log2 units; with per-block descales m is held in those units
+      float cj = cl2, vr = 1.0f, vr_inv = 1.0f;  // vr = v_j / v_max (per-block descales)
+      if constexpr (BLOCK) {
+        cj = p.scale_log2 * q_ds * k_next;
+        vr = v_next * v_inv;
+        vr_inv = __fdividef(v_max, v_next);
+        if (j + 1 < n_of(t)) {
+          k_next = p.k_bs[kvb + j + 1];
+          v_next = p.v_bs[kvb + j + 1];
+        }
+      }
+      const float mx = BLOCK ? rowmax128(s) * cj : rowmax128(s);
+      const float mdiff = BLOCK ? 1.0f : cl2;  // log2 units per unit of m
       if (j == 0) {
         m = mx;
-      } else if (__any_sync(FULL, (mx - m) * cl2 > kTau)) {
+      } else if (__any_sync(FULL, (mx - m) * mdiff > kTau)) {
         const float m_new = fmaxf(m, mx);
-        const float alpha = f8_ex2((m - m_new) * cl2);
+        const float alpha = f8_ex2((m - m_new) * mdiff);
         m = m_new;
         l *= alpha;
 #pragma unroll
@@ -339,8 +369,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
       }
       // the pre-scale of P is folded into the exponent: p = exp2(s c - m c + 7); l sums
       // the scaled values too, so it cancels in O / l (and lse subtracts 7 ln 2)
-      const float neg = -m * cl2 + kPScaleLog2;
-      const uint64_t cl2x2 = f2pack(cl2, cl2), negx2 = f2pack(neg, neg);
+      const float neg = BLOCK ? -m + kPScaleLog2 + __log2f(vr) : -m * cl2 + kPScaleLog2;
+      const uint64_t cl2x2 = f2pack(cj, cj), negx2 = f2pack(neg, neg);
       uint64_t acc0 = 0ull, acc1 = 0ull;
       uint32_t pk[32];
 #pragma unroll
@@ -359,7 +389,10 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
       float sa, sb, sc2, sd;
       f2unpack(acc0, sa, sb);
       f2unpack(acc1, sc2, sd);
-      l += (sa + sb) + (sc2 + sd);
+      if constexpr (BLOCK)
+        l += ((sa + sb) + (sc2 + sd)) * vr_inv;
+      else
+        l += (sa + sb) + (sc2 + sd);
       tmem_st32(s_tm, pk);
       tmem_wait_st();
       tc_fence_before();
@@ -374,7 +407,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
       named_bar_sync_n(1 + t, 128);
       if (wg_fail[t] == 0) {
         tc_fence_after();
-        const float f = p.out_scale / l;
+        const float f = (BLOCK ? v_max : p.out_scale) / l;
         uint16_t* orow = p.o + ((static_cast<long long>(b) * N + row) * p.Hq + h) * kD;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
@@ -393,7 +426,8 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_fp8_kernel(const __grid_constan
           }
         }
         if (row < N)
-          p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] = m * p.score_scale + logf(l) - kPScaleLog2 * kLn2;
+          p.lse[(static_cast<size_t>(b) * p.Hq + h) * N + row] =
+              (BLOCK ? m * kLn2 : m * p.score_scale) + logf(l) - kPScaleLog2 * kLn2;
       }
     }
   }
@@ -413,10 +447,14 @@ cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = causal ? fa_fwd_fp8_kernel<true> : fa_fwd_fp8_kernel<false>;
+  const bool block = p.q_bs != nullptr;
+  auto kern = causal ? (block ? fa_fwd_fp8_kernel<true, true> : fa_fwd_fp8_kernel<true, false>)
+                     : (block ? fa_fwd_fp8_kernel<false, true> : fa_fwd_fp8_kernel<false, false>);
   constexpr int kSplit = 128 * 80 + 256 * 208;
-  cudaError_t e = causal ? prepare_launch_once<fa_fwd_fp8_kernel<true>>(kSmem, 384, kSplit)
-                         : prepare_launch_once<fa_fwd_fp8_kernel<false>>(kSmem, 384, kSplit);
+  cudaError_t e = causal ? (block ? prepare_launch_once<fa_fwd_fp8_kernel<true, true>>(kSmem, 384, kSplit)
+                                  : prepare_launch_once<fa_fwd_fp8_kernel<true, false>>(kSmem, 384, kSplit))
+                         : (block ? prepare_launch_once<fa_fwd_fp8_kernel<false, true>>(kSmem, 384, kSplit)
+                                  : prepare_launch_once<fa_fwd_fp8_kernel<false, false>>(kSmem, 384, kSplit));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((p.N + 255) / 256) * p.B * p.Hq;
   kern<<<static_cast<unsigned>(grid), kThreads, kSmem, stream>>>(p);

@@ -113,6 +113,14 @@ struct Fp8Params {
   float score_scale;        // scale * q_descale * k_descale
   float out_scale;          // v_descale (P and its row sum both carry a 2^8 pre-scale)
   uint64_t wait_limit_ns;
+  // per-block descales (fa_fwd_fp8_blockscaled; null for one descale per tensor): one fp32
+  // per 128-row block of each head, q_bs [B, Hq, nb], k_bs and v_bs [B, Hkv, nb],
+  // nb = ceil(N / 128)
+  const float* q_bs;
+  const float* k_bs;
+  const float* v_bs;
+  int nb;
+  float scale_log2;  // scale * log2(e)
 };
 cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream);
 // 4-D map over an 8-bit [B, N, H, d] tensor, box {d, 1, rows, 1} (d = 128 bytes).

@@ -66,6 +66,8 @@ def _load():
     lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_fp8_workspace_size.argtypes = [i] * 4
     lib.fa_fwd_fp8_workspace_size.restype = sz
+    lib.fa_fwd_fp8_blockscaled.argtypes = [vp] * 8 + [i] * 6 + [f, vp, sz, vp]
+    lib.fa_fwd_fp8_blockscaled.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_exp2.argtypes = [vp, vp, vp, i, vp]
@@ -166,6 +168,13 @@ def fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, q_descale, k_de
 
 def fa_fwd_fp8_workspace_size(B, Hkv, N, d) -> int:
     return int(lib.fa_fwd_fp8_workspace_size(B, Hkv, N, d))
+
+
+def fa_fwd_fp8_blockscaled(q, k, v, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, N, d, causal, scale,
+                           workspace, workspace_bytes, stream) -> int:
+    """Mirror of the C ``fa_fwd_fp8_blockscaled``; the descales are device pointers."""
+    return lib.fa_fwd_fp8_blockscaled(q, k, v, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, N, d,
+                                      int(causal), float(scale), workspace, int(workspace_bytes), stream)
 
 
 def fa_selftest_wait_timeout(limit_us, stream) -> int:
@@ -336,6 +345,36 @@ def forward_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=No
                     k_descale, v_descale, _ptr(workspace), workspace.numel(), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_fp8")
+    return o, lse
+
+
+def forward_fp8_blockscaled(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=None, out=None, lse=None,
+                            workspace=None, stream=None):
+    """FP8 forward with one descale per 128-row block of each head: q [B,N,Hq,128], k/v
+    [B,N,Hkv,128] 8-bit E4M3 CUDA tensors; q_descale [B,Hq,ceil(N/128)], k_descale and
+    v_descale [B,Hkv,ceil(N/128)] fp32 CUDA tensors.  Returns (o bf16, lse fp32)."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,N,Hq,d], k and v [B,N,Hkv,d]")
+    for t in (q, k, v):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous 8-bit CUDA tensors")
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    nb = (N + 127) // 128
+    for t, hh in ((q_descale, Hq), (k_descale, Hkv), (v_descale, Hkv)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, hh, nb):
+            raise ValueError("descales must be contiguous fp32 CUDA tensors [B, H, ceil(N/128)]")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = fa_fwd_fp8_workspace_size(B, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = fa_fwd_fp8_blockscaled(_ptr(q), _ptr(k), _ptr(v), _ptr(q_descale), _ptr(k_descale), _ptr(v_descale),
+                                _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, causal, scale, _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8_blockscaled")
     return o, lse
 
 

@@ -11,6 +11,8 @@ The workload family is the one the FlashAttention-2 pages benchmark
 
 from __future__ import annotations
 
+import math
+
 import torch
 
 DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
@@ -81,6 +83,29 @@ def make_decode_inputs(B, Nq, Nmax, Hq, Hkv, d, dtype="bf16", seed=0):
     k = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
     v = torch.randn((B, Nmax, Hkv, d), generator=g, dtype=torch.float32)
     return {"q": q.to(tdt), "k": k.to(tdt), "v": v.to(tdt)}
+
+
+def make_fp8_block_inputs(B, N, Hq, Hkv, d, seed=0, spread=4.0):
+    """E4M3 inputs with one descale per 128-row block of each head: q, k, v fp32 normals
+    from one CPU generator, each 128-row block of each head multiplied by its own factor
+    drawn log-uniformly from [1/spread, spread] (so the blocks' ranges differ), divided by
+    the block's descale = block amax / 448 and rounded to nearest E4M3.  Returns a dict with
+    CPU tensors q, k, v (E4M3) and q_descale [B, Hq, nb], k_descale and v_descale
+    [B, Hkv, nb] (fp32, nb = ceil(N / 128)); real value = E4M3 value x its block's descale."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    nb = (N + 127) // 128
+    out = {}
+    for name, H in (("q", Hq), ("k", Hkv), ("v", Hkv)):
+        x = torch.randn((B, N, H, d), generator=g, dtype=torch.float32)
+        f = torch.exp((torch.rand((B, nb, H), generator=g) * 2.0 - 1.0) * math.log(spread))
+        x = x * f.repeat_interleave(128, dim=1)[:, :N, :, None]
+        xb = torch.zeros((B, nb * 128, H, d), dtype=torch.float32)
+        xb[:, :N] = x
+        amax = xb.abs().reshape(B, nb, 128, H, d).amax(dim=(2, 4))  # [B, nb, H]
+        ds = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        out[name] = (x / ds.repeat_interleave(128, dim=1)[:, :N, :, None]).to(torch.float8_e4m3fn)
+        out[name + "_descale"] = ds.permute(0, 2, 1).contiguous()  # [B, H, nb]
+    return out
 
 
 def make_fp8_inputs(B, N, Hq, Hkv, d, seed=0):

@@ -289,6 +289,25 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
                      void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * FP8 (E4M3) forward with one descale per 128-row block of each head instead of one per
+ * tensor (a reading of the same page: block scaling keeps a block of large values from
+ * costing the rest of the tensor its precision).
+ *   q_descale: DEVICE fp32 [B, Hq, nb], k_descale and v_descale: DEVICE fp32 [B, Hkv, nb],
+ *   nb = ceil(N / 128); rows [128 i, 128 i + 128) of head h of batch b have real value =
+ *   stored E4M3 value x descale[b, h, i].  Every entry must be finite and > 0 (not
+ *   checked; a value outside that range gives undefined results, not an error).
+ * The scores take the query block's and the key block's descales; P is rounded to E4M3
+ * as P * 2^7 * v_j / v_max (v_j the key block's V descale, v_max the largest among the
+ * blocks a query tile visits), and the row sum and O / l undo that factor, so a key block
+ * whose V descale is far below the largest loses P's low values to the subnormal range
+ * first.  Other arguments, workspace and conventions as fa_fwd_fp8.
+ */
+fa_status fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, const float* q_descale,
+                                 const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq,
+                                 int Hkv, int N, int d, int causal, float scale, void* workspace,
+                                 size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Size of the scratch array inside the library that fa_bwd_noalloc uses (32 MiB).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -281,6 +281,22 @@ def test_fp8_argument_errors_need_no_device(lib):
         assert fn(*a) == code, (idx, val)
 
 
+def test_fp8_blockscaled_argument_errors_need_no_device(lib):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn = lib.fa_fwd_fp8_blockscaled
+    fn.argtypes = [vp] * 8 + [i] * 6 + [f, vp, ctypes.c_size_t, vp]
+    fn.restype = i
+    base = [0x10000, 0x20000, 0x30000, 0x40000, 0x40100, 0x40200, 0x50000, 0x60000, 2, 4, 4, 300, 128, 1, 0.088,
+            0x100000, 2 * 4 * 128 * 384, None]
+    # null or misaligned tensors / descales, d != 128, bad scale, short or null workspace,
+    # Hq % Hkv != 0: rejected before any CUDA call
+    for idx, val, code in [(0, None, 1), (3, None, 1), (5, 0x40202, 1), (6, 0x50008, 1), (12, 64, 2),
+                           (14, 0.0, 1), (15, None, 1), (16, 1024, 1), (10, 3, 1)]:
+        a = list(base)
+        a[idx] = val
+        assert fn(*a) == code, (idx, val)
+
+
 def test_noalloc_scratch_limit_needs_no_device(lib):
     """fa_bwd_noalloc's fixed scratch: with B=1, Hq=16, d=128 the backward workspace fits
     up to N=4032 (Npad 4032) and not at N=4033 (Npad 4096); there the call is rejected
