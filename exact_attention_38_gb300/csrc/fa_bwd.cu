@@ -402,11 +402,17 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
 
   // ---- work decode: key blocks of one (batch, key/value head) are consecutive CTAs
   // (ascending, so with the causal mask the heaviest come first); the CTAs resident
-  // at any time then share a few heads' Q, dO and dQ accumulator through L2.
+  // at any time then share a few heads' Q, dO and dQ accumulator through L2.  With the
+  // mask, a fixed length of at least 32 key blocks and at most 64 (batch, key/value head)
+  // pairs, key block jb of every head comes before jb + 1 of any: heaviest first over the
+  // whole grid, which balances the last wave better (measured: 16k tokens 2.25 -> 2.19 ms,
+  // GQA 32 / 8 heads 4.55 -> 4.40); with more, shorter heads the head-by-head order wins.
   const int N = VARLEN ? p.vl.max_k : p.N;  // key rows the grid covers per sequence
   const int nkb = (N + 127) / 128;
-  const int jb = static_cast<int>(blockIdx.x % nkb);
-  const int bhk = static_cast<int>(blockIdx.x / nkb);
+  const int BHK = p.B * p.Hkv;
+  const bool kb_major = CAUSAL && !VARLEN && nkb >= 32 && BHK <= 64;
+  const int jb = static_cast<int>(kb_major ? blockIdx.x / BHK : blockIdx.x % nkb);
+  const int bhk = static_cast<int>(kb_major ? blockIdx.x % BHK : blockIdx.x / nkb);
   const int hkv = bhk % p.Hkv;
   const int b = bhk / p.Hkv;
   const int G = p.Hq / p.Hkv;
