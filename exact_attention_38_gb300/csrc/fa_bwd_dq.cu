@@ -3,7 +3,7 @@
 // The main backward kernel owns a block of keys and adds its dS K contribution into an
 // fp32 dQ accumulator with tensor-memory-access reductions; the order in which CTAs
 // land their additions varies from run to run, so dQ's last bits do too.  This kernel
-// instead owns a tile of 128 queries and walks the key blocks in ascending order,
+// instead owns 256 queries (two tiles of 128) and walks the key blocks in ascending order,
 // recomputing S = Q K^T and dP = dO V^T and accumulating dQ = scale * sum_j dS_j K_j in
 // tensor memory: every dQ element is then summed in the same order on every run.  The
 // price is two more GEMM-shaped products per (query, key) block (S and dP are computed
@@ -18,7 +18,7 @@
 //    once the tile's warpgroup has turned S into P = exp2(s * scale * log2 e - lse * log2 e)
 //    in its registers, dP_t = dO_t V_j^T overwrites it; the warpgroup then writes
 //    dS = P * (dP - D) as 16-bit pairs into the buffer's first 64 columns, the A operand of
-//    dQ_t += dS_t K_j (K MN-major), accumulated in the tile's own 128 TMEM columns over the
+//    dQ_t += dS_t K_j (K MN-major), accumulated in the tile's own D TMEM columns over the
 //    key blocks in ascending order;
 //  * warp 9 issues dP_0(j) dP_1(j) dQ_0(j) S_0(j+1) dQ_1(j) S_1(j+1), so each tile's softmax
 //    work runs while the tensor cores work on the other tile;
