@@ -94,7 +94,8 @@ def kernel_source_digest(kernel):
     import hashlib
 
     csrc = os.path.join(ROOT, "exact_attention_38_gb300", "csrc")
-    files = {"fa_fwd_kernel": ["fa_fwd.cu", "fa_math.cuh", "exp2_poly.h"], "fa_bwd_main": ["fa_bwd.cu"]}[kernel]
+    files = {"fa_fwd_kernel": ["fa_fwd.cu", "fa_math.cuh", "exp2_poly.h"],
+             "fa_bwd_main": ["fa_bwd.cu", "fa_bwd_common.cuh"]}[kernel]
     h = hashlib.sha256()
     for f in files + ["sm100_ptx.cuh", "fa_internal.h"]:
         with open(os.path.join(csrc, f), "rb") as fh:
@@ -474,12 +475,15 @@ def run_native(a):
         short = w["N"] <= (1024 if w.get("causal") else 512)
         kern, timed = ("fa_fwd_persistent" if short else "fa_fwd_kernel"), "one fa_fwd call (one launch)"
     elif w.get("deterministic"):
-        kern = "fa_bwd_main+fa_bwd_dq_kernel"
-        timed = ("one fa_bwd_deterministic call: preprocess + fa_bwd_main without its dQ path + fa_bwd_dq_kernel "
+        # the key-block kernel is the persistent one for N <= 512
+        kb = "fa_bwd_persistent" if w["N"] <= 512 else "fa_bwd_main"
+        kern = kb + "+fa_bwd_dq_kernel"
+        timed = (f"one fa_bwd_deterministic call: preprocess + {kb} without its dQ path + fa_bwd_dq_kernel "
                  "(FLOPs by the 2.5x backward count; the two kernels execute 3.5x the forward's)")
     else:
-        kern = "fa_bwd_main"
-        timed = "one fa_bwd call: preprocess + fa_bwd_main + dQ convert (the main kernel is ~99% of it)"
+        kern = "fa_bwd_persistent" if w["N"] <= 512 else "fa_bwd_main"
+        timed = (f"one fa_bwd call: preprocess + {kern} + dQ convert (the key-block kernel is ~98% of it at "
+                 "16k-token sequences, ~72% at N=512)")
     roofline = {"bound": "tensor", "kernel": kern, "timed": timed,
                 "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                 "traffic": (recorded_traffic(kern, workload_name(w, "step"))

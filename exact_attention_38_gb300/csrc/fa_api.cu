@@ -409,9 +409,11 @@ fa_status bwd_fixed(const void* q, const void* k, const void* v, const void* o, 
   const BwdWorkspace ws = bwd_workspace_layout(B, Hq, N, d);
   if (workspace_bytes < ws.total) return FA_ERR_INVALID;
   BwdParams p{};
+  const int out_rows = bwd_persistent(N, causal != 0) ? 32 : 128;
   if (!encode_bshd_map(&p.tm_q, q, B, N, Hq, d, 64, dtype) || !encode_bshd_map(&p.tm_do, dout, B, N, Hq, d, 64, dtype) ||
       !encode_bshd_map(&p.tm_k, k, B, N, Hkv, d, 128, dtype) || !encode_bshd_map(&p.tm_v, v, B, N, Hkv, d, 128, dtype) ||
-      !encode_bshd_map(&p.tm_dk, dk, B, N, Hkv, d, 128, dtype) || !encode_bshd_map(&p.tm_dv, dv, B, N, Hkv, d, 128, dtype))
+      !encode_bshd_map(&p.tm_dk, dk, B, N, Hkv, d, out_rows, dtype) ||
+      !encode_bshd_map(&p.tm_dv, dv, B, N, Hkv, d, out_rows, dtype))
     return FA_ERR_CUDA;
   p.err = device_error_word();
   if (!p.err) return FA_ERR_CUDA;

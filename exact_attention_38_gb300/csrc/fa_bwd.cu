@@ -32,13 +32,12 @@
 // because the tensor cores read shared-memory operands at 128 B/clk per SM and every other
 // shared-memory access competes with them.
 #include "fa_internal.h"
+#include "fa_bwd_common.cuh"
 #include "sm100_ptx.cuh"
 
 #include <cuda_fp16.h>
 
 namespace fa {
-
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
@@ -88,50 +87,6 @@ struct BwdCfg {
   static constexpr uint32_t T_S = 0, T_DP = 128, T_V = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
-
-__device__ __forceinline__ float bw_ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t bw_pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-template <bool BF16>
-__device__ __forceinline__ float bw_unpack_lo(uint32_t v) {
-  if (BF16) return __uint_as_float(v << 16);
-  __half_raw hr;
-  hr.x = static_cast<unsigned short>(v & 0xFFFFu);
-  return __half2float(__half(hr));
-}
-
-template <bool BF16>
-__device__ __forceinline__ float bw_unpack_hi(uint32_t v) {
-  if (BF16) return __uint_as_float(v & 0xFFFF0000u);
-  __half_raw hr;
-  hr.x = static_cast<unsigned short>(v >> 16);
-  return __half2float(__half(hr));
-}
-
-// global[p] += v, relaxed, without a result (a reduction, not a returning atomic)
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // ------------------------------------------------------------------- preprocess
 // -D = -rowsum(dO * O) and -lse * log2(e) in the padded [B*Hq, Npad] layout (negated so
@@ -681,20 +636,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       if (!__all_sync(FULL, mbar_wait(kv_full, 0, abort_flag, lim))) {
         ok = false;
       } else {
-#pragma unroll
-        for (int ch = 0; ch < C::CHUNKS; ++ch) {
-          uint32_t kr[32];
-          const uint8_t* rowp = smem + C::OFF_V + ch * C::KV_CHUNK + r * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(rowp + ((u ^ (r & 7)) * 16));
-            kr[4 * u] = q4.x;
-            kr[4 * u + 1] = q4.y;
-            kr[4 * u + 2] = q4.z;
-            kr[4 * u + 3] = q4.w;
-          }
-          tmem_st32(tbase + lane_off + C::T_V + 32u * ch, kr);
-        }
+        bwd_v_to_tmem<C::CHUNKS>(smem + C::OFF_V, r, tbase + lane_off + C::T_V);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(v_tmem);
@@ -733,47 +675,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       // warpgroup writes 16-byte units [4 wg, 4 wg + 4)
       uint8_t* rowp = smem + C::OFF_DS + bb * C::DS_TILE + r * 128;
       uint32_t pk[16], dsk[16];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t* dk2 = dsk + 4 * g;
-#pragma unroll
-        for (int h4 = 0; h4 < 2; ++h4) {
-          const int c4 = 2 * g + h4;
-          const float4 L = nl4[c4], Dn = nd4[c4];
-          // x = s * scale*log2(e) - lse*log2(e), two columns per instruction
-          const uint64_t x01 = ffma2(f2pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), cl2x2,
-                                     f2pack(L.x, L.y));
-          const uint64_t x23 = ffma2(f2pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])),
-                                     cl2x2, f2pack(L.z, L.w));
-          float p0, p1, p2, p3;
-          f2unpack(x01, p0, p1);
-          f2unpack(x23, p2, p3);
-          p0 = bw_ex2(p0);
-          p1 = bw_ex2(p1);
-          p2 = bw_ex2(p2);
-          p3 = bw_ex2(p3);
-          if (CAUSAL || VARLEN) {
-            if (4 * c4 + 0 < cmin) p0 = 0.f;
-            if (4 * c4 + 1 < cmin) p1 = 0.f;
-            if (4 * c4 + 2 < cmin) p2 = 0.f;
-            if (4 * c4 + 3 < cmin) p3 = 0.f;
-          }
-          // dS = P * (dP - D)
-          const uint64_t t01 = fadd2(f2pack(__uint_as_float(dpv[4 * c4]), __uint_as_float(dpv[4 * c4 + 1])),
-                                     f2pack(Dn.x, Dn.y));
-          const uint64_t t23 = fadd2(f2pack(__uint_as_float(dpv[4 * c4 + 2]), __uint_as_float(dpv[4 * c4 + 3])),
-                                     f2pack(Dn.z, Dn.w));
-          float d0, d1, d2, d3;
-          f2unpack(fmul2(f2pack(p0, p1), t01), d0, d1);
-          f2unpack(fmul2(f2pack(p2, p3), t23), d2, d3);
-          pk[2 * c4] = bw_pack2<BF16>(p0, p1);
-          pk[2 * c4 + 1] = bw_pack2<BF16>(p2, p3);
-          dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
-          dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
-        }
-        if (DQ)  // the shared-memory copy of dS^T feeds only the dQ^T product
-          *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);
-      }
+      bwd_p_ds<BF16, CAUSAL || VARLEN, DQ>(sv, dpv, nl4, nd4, cmin, cl2x2, rowp, wg, r, pk, dsk);
       // P^T (16 packed columns) then dS^T (16) go back into the 32 columns of S^T this
       // warpgroup read, so neither warpgroup writes columns the other still reads
       tmem_st16(tbase + lane_off + C::T_S + 64u * bb + cbase, pk);
@@ -921,7 +823,9 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e_side == cudaSuccess) e_side = ej;
   }
   cudaError_t e_main = cudaSuccess;
-  {
+  if (!VARLEN && bwd_persistent(p.N, CAUSAL)) {
+    e_main = launch_bwd_persistent(p, D, BF16, CAUSAL, DQ, stream);
+  } else {
     auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
     e_main = prepare_launch_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM, C::THREADS, 128 * 80 + 256 * 160 + 128 * 112);
     const long long nk = VARLEN ? p.vl.max_k : p.N;

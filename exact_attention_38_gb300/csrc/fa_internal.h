@@ -60,7 +60,8 @@ bool encode_thd_map(CUtensorMap* map, const void* base, int total, int H, int d,
 struct BwdParams {
   CUtensorMap tm_q, tm_do;  // [B, N, Hq, d], box rows 64
   CUtensorMap tm_k, tm_v;   // [B, N, Hkv, d], box rows 128
-  CUtensorMap tm_dk, tm_dv; // fixed length: outputs [B, N, Hkv, d], box rows 128 (TMA stores)
+  CUtensorMap tm_dk, tm_dv; // fixed length: outputs [B, N, Hkv, d] (TMA stores), box rows 128, or 32 for the
+                            // persistent kernel (each warp stores its own 32 key rows)
   CUtensorMap tm_dq;        // d=64: fp32 dQ accumulator [B*Hq, d, Npad], box {32, d, 1}, 128-byte swizzle
   const uint16_t* o;        // [B, N, Hq, d] (preprocess)
   const uint16_t* dout;     // [B, N, Hq, d] (preprocess)
@@ -201,6 +202,16 @@ cudaError_t launch_fwd_persistent(const FwdParams& p, int d, fa_dtype dtype, boo
 cudaError_t launch_bwd(const BwdParams& p, int d, fa_dtype dtype, bool causal, bool varlen, bool deterministic,
                        cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, fa_dtype dtype, bool causal, cudaStream_t stream);
+// Persistent form of the key-block backward kernel (fixed length; fa_bwd_persist.cu): one
+// CTA per SM takes (batch, key/value head, key block) units from a counter pair of the
+// ring above.  dq = false leaves out the dQ path, as the deterministic pass wants.  The
+// backward uses it up to these sequence lengths and one CTA per key block above.
+constexpr int kPersistentBwdMaxN = 512;
+constexpr int kPersistentBwdMaxNCausal = 512;
+inline bool bwd_persistent(int N, bool causal) {
+  return N <= (causal ? kPersistentBwdMaxNCausal : kPersistentBwdMaxN);
+}
+cudaError_t launch_bwd_persistent(const BwdParams& p, int d, bool bf16, bool causal, bool dq, cudaStream_t stream);
 
 // Geometry of sequence b of a variable-length launch; false if its offsets or length
 // contradict the launch's sizes.

@@ -41,9 +41,10 @@
  *    device, including one that has not finished when the check reads the word.
  *  - Calls on different streams may overlap; the library keeps no per-call state,
  *    except fa_bwd_noalloc, whose calls all share one scratch array and must be
- *    serialised (see there), fa_fwd's persistent kernel, whose launches each take a
- *    counter pair from a ring of 256 (see fa_fwd), and fa_bwd_deterministic, whose calls
- *    each take an event pair from a ring of 64 for its side stream (see there).
+ *    serialised (see there), the persistent kernels of fa_fwd and of the backward
+ *    passes for short sequences, whose launches each take a counter pair from a ring of
+ *    256 (see fa_fwd), and fa_bwd_deterministic, whose calls each take an event pair
+ *    from a ring of 64 for its side stream (see there).
  *  - Per device the library remembers a few addresses and settings (the error word's,
  *    the counter ring's and fa_bwd_noalloc's scratch addresses, each kernel's
  *    shared-memory limit, the deterministic backward's side stream and events), taken on
@@ -119,7 +120,11 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
  *                     it must not be shared by calls that may overlap.
  * The pass runs D = rowsum(dO * O), then a kernel over key blocks that recomputes
  * P from lse, accumulates dV and dK in tensor memory and adds dS K into the fp32
- * dQ accumulator, then converts dQ to dtype.
+ * dQ accumulator, then converts dQ to dtype.  Short sequences (N <= 512) run the key
+ * blocks in a persistent kernel: one CTA per SM takes (batch, key/value head, 128-key
+ * block) units from a counter pair of the ring fa_fwd's persistent kernel uses (same
+ * rules).  Longer sequences run one CTA per key block.  For a key block both kernels
+ * issue the same products in the same order, so dk and dv agree bit for bit.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
