@@ -20,8 +20,9 @@
 //  * warpgroup 1 copies V into TMEM as soon as the previous unit's last dP^T has been
 //    read; warpgroup 2 (the dQ^T reader) reads dK and dV out of TMEM after each unit's
 //    last gradient products, frees the accumulators for the next unit's first ones, and
-//    stores dK and dV through the finished unit's K buffer (each warp its 32 key rows,
-//    TMA stores), which then goes back to the producer.
+//    stores dK through the finished unit's K buffer and dV through the V buffer (whose
+//    next unit's V is by then in TMEM), each warp its 32 key rows by TMA stores, before
+//    both buffers go back to the producer.
 // Units are taken in the order of the one-CTA-per-block grid (with the causal mask the
 // heaviest first), so the dynamic counter balances the tail.  The counter pair {next,
 // done} is picked per launch from the ring the persistent forward uses; the last CTA to
