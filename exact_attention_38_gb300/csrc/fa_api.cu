@@ -429,6 +429,10 @@ fa_status bwd_fixed(const void* q, const void* k, const void* v, const void* o, 
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
   if (!deterministic && d == 64 && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d))
     return FA_ERR_CUDA;
+  // room for the wave-tail split's fp32 dK / dV partials (see BwdParams)
+  p.part_space = deterministic ? reinterpret_cast<float*>(w + ws.dq_acc_off) : static_cast<float*>(dq);
+  p.part_bytes = deterministic ? ws.dvec_off - ws.dq_acc_off
+                               : static_cast<size_t>(B) * N * Hq * d * 2;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -151,6 +151,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __grid_constant__
   const long long nacc4 = p.dq_acc ? static_cast<long long>(p.B) * p.Hq * D * p.Npad / 4 : 0;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (long long i = tid; i < nacc4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // wave-tail split: the fp32 dK / dV partials = 0
+  const long long npart4 = static_cast<long long>(p.nsplit) * 2 * 128 * D / 4;
+  float4* part4 = reinterpret_cast<float4*>(p.kv_part);
+  for (long long i = tid; i < npart4; i += nthreads) part4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Variable-length form: rows (b*Hq + h, n) of the padded layout, n < Npad; query n of
@@ -322,6 +326,65 @@ __device__ __forceinline__ void bwd_write_tile(uint32_t tm, float mul, uint8_t* 
   }
 }
 
+// Adds the fp32 128-key tile held in TMEM columns [col, col + D) (thread r = key row r) into
+// tile `idx` of the wave-tail split's partials (tensor map over [2 nsplit][128][D] fp32):
+// staged as 32-column chunks of 128 rows x 128 B (128-byte swizzle), then one TMA tensor
+// reduction per chunk; the 128 threads of the calling warpgroup take part (named barrier
+// `bar_id`).
+template <int D>
+__device__ __forceinline__ void bwd_add_partial(uint32_t tm, uint8_t* stage, const CUtensorMap* map, int idx,
+                                                int bar_id, int r) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tm + 32u * c, v);
+    tmem_wait_ld();
+    uint8_t* rowp = stage + c * (128 * 128) + r * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+  }
+  fence_proxy_async_smem();
+  named_bar_sync_n(bar_id, 128);
+  if (r == 0) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(map, smem_u32(stage + c * (128 * 128)), 32 * c, 0, idx);
+    bulk_commit_group();
+    bulk_wait_group_read0();  // the staging must outlive the reductions' reads of it
+  }
+}
+
+// dk / dv of the wave-tail split's key blocks: the sum of the two halves' fp32 partials,
+// dK times the scale, rounded to 16 bits.  One thread per 8 columns of a row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_split_convert(const __grid_constant__ BwdParams p) {
+  constexpr int G8 = D / 8;
+  const int nkb = (p.N + 127) / 128;
+  const long long total = static_cast<long long>(p.nsplit) * 2 * 128 * G8;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const int g8 = static_cast<int>(i % G8);
+    const int row = static_cast<int>((i / G8) % 128);
+    const int tile = static_cast<int>(i / (G8 * 128));  // 2 * split + (0: dK, 1: dV)
+    const int unit = p.split_first + tile / 2;
+    const int jb = unit % nkb, bhk = unit / nkb;
+    const int key = 128 * jb + row;
+    if (key >= p.N) continue;
+    const float* src = p.kv_part + (static_cast<long long>(tile) * 128 + row) * D + 8 * g8;
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 c = *reinterpret_cast<const float4*>(src + 4);
+    const float mul = (tile & 1) ? 1.0f : p.scale;
+    uint4 o;
+    o.x = bw_pack2<BF16>(a.x * mul, a.y * mul);
+    o.y = bw_pack2<BF16>(a.z * mul, a.w * mul);
+    o.z = bw_pack2<BF16>(c.x * mul, c.y * mul);
+    o.w = bw_pack2<BF16>(c.z * mul, c.w * mul);
+    uint16_t* out = (tile & 1) ? p.dv : p.dk;
+    const int hkv = bhk % p.Hkv, b = bhk / p.Hkv;
+    *reinterpret_cast<uint4*>(out + ((static_cast<long long>(b) * p.N + key) * p.Hkv + hkv) * D + 8 * g8) = o;
+  }
+}
+
 // ------------------------------------------------------------------- main kernel
 template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
 __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ BwdParams p) {
@@ -366,8 +429,16 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   const int nkb = (N + 127) / 128;
   const int BHK = p.B * p.Hkv;
   const bool kb_major = CAUSAL && !VARLEN && nkb >= 32 && BHK <= 64;
-  const int jb = static_cast<int>(kb_major ? blockIdx.x / BHK : blockIdx.x % nkb);
-  const int bhk = static_cast<int>(kb_major ? blockIdx.x % BHK : blockIdx.x / nkb);
+  // Wave-tail split (fixed length, non-causal): the grid's last nsplit key blocks would
+  // run on a fraction of the SMs after the others are done, so each runs as two CTAs,
+  // half of the query walk each (half = 0, 1; -1 for a whole walk).
+  int unit = static_cast<int>(blockIdx.x), half = -1;
+  if (!CAUSAL && !VARLEN && p.nsplit > 0 && unit >= p.split_first) {
+    half = (unit - p.split_first) & 1;
+    unit = p.split_first + ((unit - p.split_first) >> 1);
+  }
+  const int jb = kb_major ? unit / BHK : unit % nkb;
+  const int bhk = kb_major ? unit % BHK : unit / nkb;
   const int hkv = bhk % p.Hkv;
   const int b = bhk / p.Hkv;
   const int G = p.Hq / p.Hkv;
@@ -387,7 +458,9 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
   const int nqb = (len_q + 63) / 64;
   const int qb0 = CAUSAL ? (VARLEN ? max(0, k0 - off) / 64 : 2 * jb) : 0;
   const int nq = max(0, nqb - qb0);  // query blocks per head
-  const int T = G * nq;              // steps of this CTA
+  // steps [it0, it0 + T) of the walk over G * nq (query head, query block) steps
+  const int it0 = half == 1 ? G * nq / 2 : 0;
+  const int T = half < 0 ? G * nq : (half == 0 ? G * nq / 2 : G * nq - G * nq / 2);
   if (VARLEN && T == 0) {
     // no query sees these keys: dK = dV = 0
     for (int i = threadIdx.x; i < 128 * (D / 8); i += blockDim.x) {
@@ -479,8 +552,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
           ok = false;
           break;
         }
-        const int hq = hkv * G + it / nq;
-        const int q0 = 64 * (qb0 + it % nq);
+        const int hq = hkv * G + (it0 + it) / nq;
+        const int q0 = 64 * (qb0 + (it0 + it) % nq);
         if (leader) {
           mbar_arrive_expect_tx(st_full(s), 2 * C::Q_TILE + 2 * 256);
           for (int ch = 0; ch < C::CHUNKS; ++ch) {
@@ -646,7 +719,7 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     }
     for (int it = 0; it < T && ok; ++it) {
       const int s = it % C::STG, bb = it & 1;
-      const int q0 = 64 * (qb0 + it % nq);
+      const int q0 = 64 * (qb0 + (it0 + it) % nq);
       if (!__all_sync(FULL, mbar_wait(st_full(s), (it / C::STG) & 1, abort_flag, lim) &&
                                 mbar_wait(sdp_full, it & 1, abort_flag, lim))) {
         ok = false;
@@ -698,9 +771,14 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
       named_bar_sync_n(2, 128);
       if (wg_fail[0] == 0) {
         tc_fence_after();
-        const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
-        bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DK, p.scale, smem + C::OFF_Q, &p.tm_dk,
-                                        p.dk + (krow * p.Hkv + hkv) * D, key < len_k, 2, r, hkv, k0, b);
+        if (half >= 0) {
+          bwd_add_partial<D>(tbase + lane_off + C::T_DK, smem + C::OFF_Q, &p.tm_kvpart, 2 * (unit - p.split_first), 2,
+                             r);
+        } else {
+          const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
+          bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DK, p.scale, smem + C::OFF_Q, &p.tm_dk,
+                                          p.dk + (krow * p.Hkv + hkv) * D, key < len_k, 2, r, hkv, k0, b);
+        }
       }
     }
   } else {
@@ -714,8 +792,8 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     // swizzle and added by one TMA tensor reduction.
     bool ok = true;
     for (int it = 0; it < (DQ ? T : 0); ++it) {  // without the dQ path only the dV epilogue
-      const int hq = hkv * G + it / nq;
-      const int q0 = 64 * (qb0 + it % nq);
+      const int hq = hkv * G + (it0 + it) / nq;
+      const int q0 = 64 * (qb0 + (it0 + it) % nq);
       const bool got = __all_sync(FULL, mbar_wait(dq_full(it & 1), (it >> 1) & 1, abort_flag, lim));
       uint32_t v[64];
       if (got) {
@@ -779,10 +857,15 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
     named_bar_sync_n(3, 128);
     if (wg_fail[2] == 0) {
       tc_fence_after();
-      const int key = k0 + r;
-      const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
-      bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DV, 1.0f, smem + C::OFF_DO, &p.tm_dv,
-                                      p.dv + (krow * p.Hkv + hkv) * D, key < len_k, 3, r, hkv, k0, b);
+      if (half >= 0) {
+        bwd_add_partial<D>(tbase + lane_off + C::T_DV, smem + C::OFF_DO, &p.tm_kvpart, 2 * (unit - p.split_first) + 1,
+                           3, r);
+      } else {
+        const int key = k0 + r;
+        const long long krow = VARLEN ? static_cast<long long>(start_k) + key : static_cast<long long>(b) * N + key;
+        bwd_write_tile<D, BF16, VARLEN>(tbase + lane_off + C::T_DV, 1.0f, smem + C::OFF_DO, &p.tm_dv,
+                                        p.dv + (krow * p.Hkv + hkv) * D, key < len_k, 3, r, hkv, k0, b);
+      }
     }
   }
 
@@ -795,9 +878,29 @@ __global__ void __launch_bounds__(512, 1) fa_bwd_main(const __grid_constant__ Bw
 }
 
 template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool DQ>
-static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+static cudaError_t launch_bwd_t(const BwdParams& args, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int sms = device_sm_count();
+  BwdParams p = args;
+  p.kv_part = nullptr;
+  p.nsplit = 0;
+  p.split_first = 0;
+  const bool persistent = !VARLEN && bwd_persistent(p.N, CAUSAL);
+  // Wave-tail split of the one-CTA-per-key-block grid (see BwdParams): when the grid's last
+  // wave would occupy at most half of the SMs, its key blocks run as two half-walk CTAs
+  // each, so that wave takes about half as long.  Needs room for the fp32 partials.
+  if (!CAUSAL && !VARLEN && !persistent && sms > 0) {
+    const long long units = static_cast<long long>((p.N + 127) / 128) * p.B * p.Hkv;
+    const long long r = units % sms;
+    const long long steps = static_cast<long long>(p.Hq / p.Hkv) * ((p.N + 63) / 64);
+    const size_t bytes = static_cast<size_t>(r) * 2 * 128 * D * 4;
+    if (r > 0 && 2 * r <= sms && steps >= 2 && p.part_space != nullptr && bytes <= p.part_bytes &&
+        encode_dq_acc_map(&p.tm_kvpart, p.part_space, static_cast<int>(2 * r), D, 128)) {
+      p.kv_part = p.part_space;
+      p.nsplit = static_cast<int>(r);
+      p.split_first = static_cast<int>(units - r);
+    }
+  }
   {
     // preprocess: LPR lanes per row, 8 rows per 256-thread block and step
     const long long rows = VARLEN ? static_cast<long long>(p.B) * p.Hq * p.Npad : static_cast<long long>(p.B) * p.N * p.Hq;
@@ -823,15 +926,23 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e_side == cudaSuccess) e_side = ej;
   }
   cudaError_t e_main = cudaSuccess;
-  if (!VARLEN && bwd_persistent(p.N, CAUSAL)) {
+  if (persistent) {
     e_main = launch_bwd_persistent(p, D, BF16, CAUSAL, DQ, stream);
   } else {
     auto kern = fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>;
     e_main = prepare_launch_once<fa_bwd_main<D, BF16, CAUSAL, VARLEN, DQ>>(C::SMEM, C::THREADS, 128 * 80 + 256 * 160 + 128 * 112);
     const long long nk = VARLEN ? p.vl.max_k : p.N;
-    const long long grid = ((nk + 127) / 128) * p.B * p.Hkv;
+    const long long grid = ((nk + 127) / 128) * p.B * p.Hkv + p.nsplit;
     if (e_main == cudaSuccess && grid > 0) {
       kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(p);
+      e_main = cudaGetLastError();
+    }
+    if (e_main == cudaSuccess && p.nsplit > 0) {
+      // the split key blocks' dk / dv, before anything overwrites the partials (with the dQ
+      // path they sit in dq, which the dQ convert below writes)
+      const long long want = (static_cast<long long>(p.nsplit) * 2 * 128 * (D / 8) + 255) / 256;
+      const int grid2 = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+      fa_bwd_split_convert<D, BF16><<<grid2, 256, 0, stream>>>(p);
       e_main = cudaGetLastError();
     }
   }

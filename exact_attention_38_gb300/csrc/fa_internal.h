@@ -77,6 +77,19 @@ struct BwdParams {
   float scale, scale_log2;
   uint64_t wait_limit_ns;
   Seqlens vl;  // varlen: packed layouts ([total, H, d] tensors, lse [Hq, total_q])
+  // Wave-tail split (fixed length, non-causal, one CTA per key block): the last nsplit key
+  // blocks of the grid run as two CTAs each, one per half of the query walk, which add
+  // their fp32 dK / dV into kv_part [nsplit][2 (dK, dV)][128][d] (zeroed by the
+  // preprocess; TMA map tm_kvpart, 3-D {d, 128, 2 nsplit}, box {32, 128, 1}), and
+  // fa_bwd_split_convert writes those blocks' dk / dv.  Key block u >= split_first runs
+  // as CTAs split_first + 2 (u - split_first) + h.  part_space / part_bytes: memory the
+  // call may use for kv_part (fa_bwd: the dq output, written only at the end;
+  // fa_bwd_deterministic: the unused fp32 dQ accumulator); null / 0 where the split is off.
+  CUtensorMap tm_kvpart;
+  float* kv_part;
+  int split_first, nsplit;
+  float* part_space;
+  size_t part_bytes;
 };
 
 // Decode-shaped forward with split keys.

@@ -124,7 +124,11 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
  * blocks in a persistent kernel: one CTA per SM takes (batch, key/value head, 128-key
  * block) units from a counter pair of the ring fa_fwd's persistent kernel uses (same
  * rules).  Longer sequences run one CTA per key block.  For a key block both kernels
- * issue the same products in the same order, so dk and dv agree bit for bit.
+ * issue the same products in the same order, so dk and dv agree bit for bit.  Without
+ * the mask, when the one-CTA-per-block grid's last wave would occupy at most half of the
+ * SMs, its key blocks run as two CTAs each (one per half of the query walk) whose fp32 dK
+ * and dV partials are summed before rounding; the partials are kept in dq's memory, which
+ * the pass writes last.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
