@@ -354,7 +354,14 @@ def run_native(a):
     parts = {"step": [("fwd", fwd), ("bwd", bwd)], "fwd": [("fwd", fwd)], "bwd": [("bwd", bwd)]}[a.which]
     if a.which == "bwd":
         fwd()
-    launches_per_step = sum({"fwd": 1, "bwd": 3}[n] for n, _ in parts)  # deterministic: preprocess, dK/dV, dQ
+    # backward: preprocess, key-block kernel, dQ convert (deterministic: dQ kernel), plus the
+    # wave-tail split's dK / dV convert when the one-CTA-per-key-block grid is split (the
+    # library's rule: non-causal, N > 512, last wave at most half of the SMs)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = B * Hkv * ((N + 127) // 128)
+    split = (not causal and N > 512 and 0 < units % sms <= sms // 2
+             and (units % sms) * 2 * 128 * d * 4 <= B * N * Hq * d * 2)
+    launches_per_step = sum({"fwd": 1, "bwd": 4 if split else 3}[n] for n, _ in parts)
 
     for _ in range(a.warmup):
         for _, fn in parts:
