@@ -31,6 +31,10 @@
 // Taking operands from TMEM, and keeping the dQ^T additions out of shared memory, matters
 // because the tensor cores read shared-memory operands at 128 B/clk per SM and every other
 // shared-memory access competes with them.
+// Without the mask, a last wave of key-block CTAs that would fill at most half the SMs is
+// split: each of its key blocks runs as two CTAs over halves of the walk, which add fp32
+// dK / dV partials that fa_bwd_split_convert then writes.  Short sequences run the same
+// steps in the persistent kernel of fa_bwd_persist.cu.
 #include "fa_internal.h"
 #include "fa_bwd_common.cuh"
 #include "sm100_ptx.cuh"
