@@ -429,10 +429,21 @@ fa_status bwd_fixed(const void* q, const void* k, const void* v, const void* o, 
   p.l2vec = reinterpret_cast<float*>(w + ws.l2vec_off);
   if (!deterministic && d == 64 && !encode_dq_acc_map(&p.tm_dq, p.dq_acc, B * Hq, (N + 63) / 64 * 64, d))
     return FA_ERR_CUDA;
-  // room for the wave-tail split's fp32 dK / dV partials (see BwdParams)
-  p.part_space = deterministic ? reinterpret_cast<float*>(w + ws.dq_acc_off) : static_cast<float*>(dq);
-  p.part_bytes = deterministic ? ws.dvec_off - ws.dq_acc_off
-                               : static_cast<size_t>(B) * N * Hq * d * 2;
+  // room for the wave-tail split's fp32 dK / dV partials (see BwdParams): fa_bwd keeps them
+  // in dq, which it otherwise writes only at the end, so not when dq's memory overlaps an
+  // input of the pass (the split would overwrite it before it is read)
+  const size_t q_bytes = static_cast<size_t>(B) * N * Hq * d * 2, kv_bytes = static_cast<size_t>(B) * N * Hkv * d * 2;
+  auto overlaps = [&](const void* a, size_t na) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(dq);
+    return x < y + q_bytes && y < x + na;
+  };
+  const bool dq_clear = !overlaps(q, q_bytes) && !overlaps(k, kv_bytes) && !overlaps(v, kv_bytes) &&
+                        !overlaps(o, q_bytes) && !overlaps(dout, q_bytes) &&
+                        !overlaps(lse, static_cast<size_t>(B) * Hq * N * 4);
+  p.part_space = deterministic ? reinterpret_cast<float*>(w + ws.dq_acc_off)
+                 : dq_clear    ? static_cast<float*>(dq)
+                               : nullptr;
+  p.part_bytes = deterministic ? ws.dvec_off - ws.dq_acc_off : dq_clear ? q_bytes : 0;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -128,7 +128,8 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
  * the mask, when the one-CTA-per-block grid's last wave would occupy at most half of the
  * SMs, its key blocks run as two CTAs each (one per half of the query walk) whose fp32 dK
  * and dV partials are summed before rounding; the partials are kept in dq's memory, which
- * the pass writes last.
+ * the pass writes last (not when dq overlaps one of the pass's inputs: then the grid is
+ * not split).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,

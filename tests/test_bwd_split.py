@@ -100,3 +100,25 @@ def test_deterministic_split(fa_lib):
             assert torch.equal(a, b)
     assert torch.equal(runs[0][1], g[1]) and torch.equal(runs[0][2], g[2])
     assert (runs[0][0].float() - g[0].float()).abs().max().item() <= 2 * ATOL["bf16"]
+
+
+def test_dq_aliasing_dout_skips_split(fa_lib):
+    """dq given the memory of dout (written only after the pass has read dout): the split,
+    which would keep its partials in dq, is skipped, and the results are the oracle's."""
+    fa = fa_lib
+    B = _pick_batch(1536, 8, 2, 8)
+    if B is None:
+        pytest.skip("no batch size in range splits on this device")
+    N, H, d = 1536, 8, 128
+    x = make_inputs(B, N, H, H, d, dtype="bf16", seed=905)
+    q, k, v, do = (to_gpu(x[n]) for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=False, scale=scale)
+    shared = do.clone()
+    dq, dk, dv = fa.backward(shared, q, k, v, o, lse, causal=False, scale=scale, dq=shared)
+    fa.check_device_error()
+    assert dq.data_ptr() == shared.data_ptr()
+    xo = {n: f64(t) for n, t in x.items()}
+    ref = oracle.attn_bwd_ref(xo["q"], xo["k"], xo["v"], xo["do"], False, scale)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(name, f64(got.cpu()), ref[name], ATOL["bf16"], "bf16")
