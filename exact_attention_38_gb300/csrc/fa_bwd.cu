@@ -237,10 +237,10 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const __grid_constant__
     const float4 a = src[0], c = src[1];
     const float sc = p.scale;
     uint4 o;
-    o.x = bw_pack2<BF16>(a.x * sc, a.y * sc);
-    o.y = bw_pack2<BF16>(a.z * sc, a.w * sc);
-    o.z = bw_pack2<BF16>(c.x * sc, c.y * sc);
-    o.w = bw_pack2<BF16>(c.z * sc, c.w * sc);
+    o.x = pack_half2<BF16>(a.x * sc, a.y * sc);
+    o.y = pack_half2<BF16>(a.z * sc, a.w * sc);
+    o.z = pack_half2<BF16>(c.x * sc, c.y * sc);
+    o.w = pack_half2<BF16>(c.z * sc, c.w * sc);
     *reinterpret_cast<uint4*>(p.dq + (orow * p.Hq + h) * D + 8 * part) = o;
   }
 }
@@ -275,10 +275,10 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_t(const __grid_constant
     const int n = i / G, g = i % G;
     if (n0 + n >= len_q) continue;
     uint4 o;
-    o.x = bw_pack2<BF16>(tile[8 * g + 0][n] * p.scale, tile[8 * g + 1][n] * p.scale);
-    o.y = bw_pack2<BF16>(tile[8 * g + 2][n] * p.scale, tile[8 * g + 3][n] * p.scale);
-    o.z = bw_pack2<BF16>(tile[8 * g + 4][n] * p.scale, tile[8 * g + 5][n] * p.scale);
-    o.w = bw_pack2<BF16>(tile[8 * g + 6][n] * p.scale, tile[8 * g + 7][n] * p.scale);
+    o.x = pack_half2<BF16>(tile[8 * g + 0][n] * p.scale, tile[8 * g + 1][n] * p.scale);
+    o.y = pack_half2<BF16>(tile[8 * g + 2][n] * p.scale, tile[8 * g + 3][n] * p.scale);
+    o.z = pack_half2<BF16>(tile[8 * g + 4][n] * p.scale, tile[8 * g + 5][n] * p.scale);
+    o.w = pack_half2<BF16>(tile[8 * g + 6][n] * p.scale, tile[8 * g + 7][n] * p.scale);
     *reinterpret_cast<uint4*>(p.dq + ((row0 + n0 + n) * p.Hq + h) * D + 8 * g) = o;
   }
 }
@@ -301,7 +301,7 @@ __device__ __forceinline__ void bwd_write_tile(uint32_t tm, float mul, uint8_t* 
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      pk[i] = bw_pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+      pk[i] = pack_half2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
     if (VARLEN) {
       if (live) {
 #pragma unroll
@@ -379,10 +379,10 @@ __global__ void __launch_bounds__(256) fa_bwd_split_convert(const __grid_constan
     const float4 c = *reinterpret_cast<const float4*>(src + 4);
     const float mul = (tile & 1) ? 1.0f : p.scale;
     uint4 o;
-    o.x = bw_pack2<BF16>(a.x * mul, a.y * mul);
-    o.y = bw_pack2<BF16>(a.z * mul, a.w * mul);
-    o.z = bw_pack2<BF16>(c.x * mul, c.y * mul);
-    o.w = bw_pack2<BF16>(c.z * mul, c.w * mul);
+    o.x = pack_half2<BF16>(a.x * mul, a.y * mul);
+    o.y = pack_half2<BF16>(a.z * mul, a.w * mul);
+    o.z = pack_half2<BF16>(c.x * mul, c.y * mul);
+    o.w = pack_half2<BF16>(c.z * mul, c.w * mul);
     uint16_t* out = (tile & 1) ? p.dv : p.dk;
     const int hkv = bhk % p.Hkv, b = bhk / p.Hkv;
     *reinterpret_cast<uint4*>(out + ((static_cast<long long>(b) * p.N + key) * p.Hkv + hkv) * D + 8 * g8) = o;

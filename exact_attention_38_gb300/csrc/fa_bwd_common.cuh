@@ -24,16 +24,6 @@ __device__ __forceinline__ float bw_ex2(float x) {
 }
 
 template <bool BF16>
-__device__ __forceinline__ uint32_t bw_pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-template <bool BF16>
 __device__ __forceinline__ float bw_unpack_lo(uint32_t v) {
   if (BF16) return __uint_as_float(v << 16);
   __half_raw hr;
@@ -127,10 +117,10 @@ __device__ __forceinline__ void bwd_p_ds(const uint32_t (&sv)[32], const uint32_
       float d0, d1, d2, d3;
       f2unpack(fmul2(f2pack(p0, p1), t01), d0, d1);
       f2unpack(fmul2(f2pack(p2, p3), t23), d2, d3);
-      pk[2 * c4] = bw_pack2<BF16>(p0, p1);
-      pk[2 * c4 + 1] = bw_pack2<BF16>(p2, p3);
-      dk2[2 * h4] = bw_pack2<BF16>(d0, d1);
-      dk2[2 * h4 + 1] = bw_pack2<BF16>(d2, d3);
+      pk[2 * c4] = pack_half2<BF16>(p0, p1);
+      pk[2 * c4 + 1] = pack_half2<BF16>(p2, p3);
+      dk2[2 * h4] = pack_half2<BF16>(d0, d1);
+      dk2[2 * h4 + 1] = pack_half2<BF16>(d2, d3);
     }
     if (DQ)  // the shared-memory copy of dS^T feeds only the dQ^T product
       *reinterpret_cast<uint4*>(rowp + (((4 * wg + g) ^ (r & 7)) * 16)) = make_uint4(dk2[0], dk2[1], dk2[2], dk2[3]);

@@ -64,16 +64,6 @@ __device__ __forceinline__ float dq_ex2(float x) {
   return y;
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t dq_pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
@@ -381,7 +371,7 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
           f2unpack(fmul2(f2pack(pv[32 * c + 2 * u], pv[32 * c + 2 * u + 1]),
                          fadd2(f2pack(__uint_as_float(dpv[2 * u]), __uint_as_float(dpv[2 * u + 1])), ndx2)),
                    d0, d1);
-          pk[u] = dq_pack2<BF16>(d0, d1);
+          pk[u] = pack_half2<BF16>(d0, d1);
         }
         tmem_st16(sd_tm + 16u * c, pk);
       }
@@ -408,10 +398,10 @@ __global__ void __launch_bounds__(384, 1) fa_bwd_dq_kernel(const __grid_constant
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 o;
-            o.x = dq_pack2<BF16>(__uint_as_float(v[8 * u + 0]) * p.scale, __uint_as_float(v[8 * u + 1]) * p.scale);
-            o.y = dq_pack2<BF16>(__uint_as_float(v[8 * u + 2]) * p.scale, __uint_as_float(v[8 * u + 3]) * p.scale);
-            o.z = dq_pack2<BF16>(__uint_as_float(v[8 * u + 4]) * p.scale, __uint_as_float(v[8 * u + 5]) * p.scale);
-            o.w = dq_pack2<BF16>(__uint_as_float(v[8 * u + 6]) * p.scale, __uint_as_float(v[8 * u + 7]) * p.scale);
+            o.x = pack_half2<BF16>(__uint_as_float(v[8 * u + 0]) * p.scale, __uint_as_float(v[8 * u + 1]) * p.scale);
+            o.y = pack_half2<BF16>(__uint_as_float(v[8 * u + 2]) * p.scale, __uint_as_float(v[8 * u + 3]) * p.scale);
+            o.z = pack_half2<BF16>(__uint_as_float(v[8 * u + 4]) * p.scale, __uint_as_float(v[8 * u + 5]) * p.scale);
+            o.w = pack_half2<BF16>(__uint_as_float(v[8 * u + 6]) * p.scale, __uint_as_float(v[8 * u + 7]) * p.scale);
             *reinterpret_cast<uint4*>(out + 32 * c + 8 * u) = o;
           }
         }

@@ -122,7 +122,7 @@ __device__ __forceinline__ void bp_stage_rows(uint32_t col, float mul, uint8_t* 
       for (int i = 0; i < 4; ++i) {
         float a = __uint_as_float(v[8 * u8 + 2 * i]), b = __uint_as_float(v[8 * u8 + 2 * i + 1]);
         if (SCALED) f2unpack(fmul2(f2pack(a, b), mul2), a, b);
-        pk[i] = bw_pack2<BF16>(a, b);
+        pk[i] = pack_half2<BF16>(a, b);
       }
       const int unit = (c0 % 64) / 8 + u8;
       *reinterpret_cast<uint4*>(rowp + ((unit ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);

@@ -53,16 +53,6 @@ __device__ __forceinline__ float dec_ex2(float x) {
   return y;
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t dec_pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Writes the result of a row that sees no key (o = 0, lse = -inf), or of an empty
 // split (partial o = 0, partial lse = -inf: weight 0 in the combine).
 template <int D>
@@ -378,7 +368,7 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
           f2unpack(ffma2(f2pack(s0, s1), cl2x2, negx2), a0, a1);
           const float p0 = dec_ex2(a0), p1 = dec_ex2(a1);
           acc = fadd2(acc, f2pack(p0, p1));
-          pk[u] = dec_pack2<BF16>(p0, p1);
+          pk[u] = pack_half2<BF16>(p0, p1);
         }
         float sa, sb;
         f2unpack(acc, sa, sb);
@@ -414,10 +404,10 @@ __global__ void __launch_bounds__(256, 2) fa_decode_kernel(const __grid_constant
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 w;
-            w.x = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
-            w.y = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
-            w.z = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
-            w.w = dec_pack2<BF16>(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
+            w.x = pack_half2<BF16>(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
+            w.y = pack_half2<BF16>(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
+            w.z = pack_half2<BF16>(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
+            w.w = pack_half2<BF16>(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
             reinterpret_cast<uint4*>(orow)[u] = w;
           }
         } else {
@@ -550,11 +540,11 @@ __global__ void __launch_bounds__(256) fa_decode_combine(const __grid_constant__
       uint16_t* orow = p.o + ((static_cast<long long>(b) * p.Nq + i) * p.Hq + h) * D + lane * V;
       if constexpr (V == 4) {
         uint2 o2;
-        o2.x = dec_pack2<BF16>(acc[0], acc[1]);
-        o2.y = dec_pack2<BF16>(acc[2], acc[3]);
+        o2.x = pack_half2<BF16>(acc[0], acc[1]);
+        o2.y = pack_half2<BF16>(acc[2], acc[3]);
         *reinterpret_cast<uint2*>(orow) = o2;
       } else {
-        *reinterpret_cast<uint32_t*>(orow) = dec_pack2<BF16>(acc[0], acc[1]);
+        *reinterpret_cast<uint32_t*>(orow) = pack_half2<BF16>(acc[0], acc[1]);
       }
       if (lane == 0) p.lse[(static_cast<long long>(b) * p.Hq + h) * p.Nq + i] = lse;
     }

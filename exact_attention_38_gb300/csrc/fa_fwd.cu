@@ -56,16 +56,6 @@ struct FwdCfg {
 
 __device__ __forceinline__ float ex2f(float x) { return ex2_mufu(x); }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -381,7 +371,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
       l += (sa + sb) + (sc2 + sd);
       uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) pk[i] = pack2<BF16>(s[2 * i], s[2 * i + 1]);
+      for (int i = 0; i < 64; ++i) pk[i] = pack_half2<BF16>(s[2 * i], s[2 * i + 1]);
       tmem_st32(s_tm, pk);
       tmem_st32(s_tm + 32u, pk + 32);
       tmem_wait_st();
@@ -414,7 +404,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_kernel(const __grid_constant__ 
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+            pk[i] = pack_half2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
           if (direct) {
             if (row < len_q) {
 #pragma unroll

@@ -70,16 +70,6 @@ struct PfCfg {
   static constexpr uint32_t TMEM_COLS = 512;  // S_0, S_1 (128 each), O_0, O_1 (D each)
 };
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pf_pack2(float lo, float hi) {
-  uint32_t r;
-  if (BF16)
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // One unit: 256 queries [256 qb, 256 qb + 256) of (b, h); tile t = rows 256 qb + 128 t,
 // visiting n_t key blocks (0 when the tile starts past N).
 struct PfUnit {
@@ -447,7 +437,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_persistent(const __grid_constan
         l += (sa + sb) + (sc2 + sd);
         uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) pk[i] = pf_pack2<BF16>(s[2 * i], s[2 * i + 1]);
+        for (int i = 0; i < 64; ++i) pk[i] = pack_half2<BF16>(s[2 * i], s[2 * i + 1]);
         tmem_st32(s_tm, pk);
         tmem_st32(s_tm + 32u, pk + 32);
         tmem_wait_st();
@@ -473,7 +463,7 @@ __global__ void __launch_bounds__(384, 1) fa_fwd_persistent(const __grid_constan
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[16 * cc + i] = pf_pack2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
+          pk[16 * cc + i] = pack_half2<BF16>(__uint_as_float(orr[2 * i]) * inv, __uint_as_float(orr[2 * i + 1]) * inv);
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_OF, t));

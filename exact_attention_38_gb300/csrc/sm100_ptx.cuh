@@ -66,6 +66,18 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Two fp32 values rounded to nearest into one 32-bit word of 16-bit floats, `lo` in the
+// low half: bf16 pairs when BF16, else fp16 pairs.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  if (BF16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // max(a, b, c) in one instruction (three-input form, sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
